@@ -1,0 +1,201 @@
+"""Seeded synthetic inputs for absorbed-MLA decode.
+
+This module only draws random numbers and lays them out; it performs none of the
+attention arithmetic.  Both the fp64 oracle tests and the CUDA path take their
+inputs from here, so the two sides always see identical bytes.
+
+Recipe (moonmath-ai/amd-kernels README, "MLA decode" usage block and the MI300X
+results table; the synthetic workloads of this library follow it):
+
+* queries ``q_lat`` / ``q_pe`` are bf16 draws of N(0, 1), shaped
+  ``[B*q_len, H, d_v]`` and ``[B*q_len, H, d_rope]`` (row ``b*q_len + t``);
+* the pool holds one fused fp8 e4m3fn row per token, the cast of
+  ``N(0, 1) / kv_scale`` with ``kv_scale = 1/32``; columns ``[0, d_v)`` are the
+  latent part (also V) and ``[d_v, d_v + d_rope)`` the RoPE part;
+* page size is 1: ``kv_indices`` is a seeded random permutation of the pool's
+  slots, ``kv_indptr`` the prefix sums of the per-request lengths;
+* ``scale = (d_v + d_rope) ** -0.5``.
+
+Everything is generated on the CPU with ``torch.Generator`` so the oracle can read
+exactly the bytes the GPU gets.  Large pools are drawn in fixed-size chunks from
+one generator, which keeps the sequence identical whatever the chunk size.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import torch
+
+D_LATENT = 512
+D_ROPE = 64
+SPARSE_D_NOPE = 448
+KV_SCALE = 1.0 / 32.0
+_CHUNK = 1 << 22  # floats drawn per step when filling a pool
+
+
+@dataclasses.dataclass
+class DenseInputs:
+    """One dense decode call's inputs (CPU tensors)."""
+
+    batch: int
+    q_len: int
+    num_heads: int
+    q_lat: torch.Tensor      # bf16 [B*q_len, H, d_v]
+    q_pe: torch.Tensor       # bf16 [B*q_len, H, d_rope]
+    pool: torch.Tensor       # uint8 [N, 1, d_v + d_rope]  (fp8 e4m3fn bytes)
+    seq_lens: torch.Tensor   # int32 [B]
+    kv_indices: torch.Tensor  # int32 [sum(seq_lens)]
+    kv_indptr: torch.Tensor  # int32 [B + 1]
+    scale: float
+    kv_scale: float
+
+    @property
+    def d_v(self) -> int:
+        return self.q_lat.shape[-1]
+
+    @property
+    def d_rope(self) -> int:
+        return self.q_pe.shape[-1]
+
+    @property
+    def total_keys(self) -> int:
+        return int(self.kv_indices.numel())
+
+
+@dataclasses.dataclass
+class SparseInputs:
+    """One sparse top-k decode call's inputs (CPU tensors)."""
+
+    num_tokens: int
+    num_heads: int
+    topk: int
+    q_nope: torch.Tensor     # bf16 [T, H, d_v]
+    q_pe: torch.Tensor       # bf16 [T, H, d_rope]
+    pool: torch.Tensor       # uint8 [N, d_v + d_rope]
+    indices: torch.Tensor    # int32 [T, topk]; negative = invalid entry
+    scale: float
+    kv_scale: float
+
+    @property
+    def d_v(self) -> int:
+        return self.q_nope.shape[-1]
+
+    @property
+    def d_rope(self) -> int:
+        return self.q_pe.shape[-1]
+
+
+def _gen(seed: int) -> torch.Generator:
+    return torch.Generator().manual_seed(int(seed))
+
+
+def _bf16_normal(shape, g: torch.Generator) -> torch.Tensor:
+    return torch.randn(*shape, generator=g).to(torch.bfloat16)
+
+
+def fp8_pool(rows: int, width: int, g: torch.Generator,
+             kv_scale: float = KV_SCALE) -> torch.Tensor:
+    """uint8 [rows, width]: e4m3fn bytes of N(0,1)/kv_scale, drawn chunk by chunk."""
+    out = torch.empty(rows * width, dtype=torch.uint8)
+    total = rows * width
+    pos = 0
+    while pos < total:
+        n = min(_CHUNK, total - pos)
+        x = torch.randn(n, generator=g) / kv_scale
+        out[pos:pos + n] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        pos += n
+    return out.view(rows, width)
+
+
+def dense_inputs(batch: int, q_len: int, num_heads: int,
+                 seq_lens: Sequence[int] | torch.Tensor,
+                 seed: int = 0, *, d_v: int = D_LATENT, d_rope: int = D_ROPE,
+                 kv_scale: float = KV_SCALE, scale: Optional[float] = None,
+                 extra_slots: int = 0) -> DenseInputs:
+    """Dense decode inputs with a shuffled page_size-1 pool.
+
+    ``extra_slots`` adds unused pool rows, so slots are a random subset of the
+    pool rather than all of it.
+    """
+    g = _gen(seed)
+    lens = torch.as_tensor(list(seq_lens) if not torch.is_tensor(seq_lens)
+                           else seq_lens, dtype=torch.int64).reshape(-1)
+    assert lens.numel() == batch
+    total = int(lens.sum())
+    rows = batch * q_len
+    q_lat = _bf16_normal((rows, num_heads, d_v), g)
+    q_pe = _bf16_normal((rows, num_heads, d_rope), g)
+    n_slots = total + int(extra_slots)
+    pool = fp8_pool(max(n_slots, 1), d_v + d_rope, g, kv_scale).view(
+        max(n_slots, 1), 1, d_v + d_rope)
+    perm = torch.randperm(max(n_slots, 1), generator=g)[:total].to(torch.int32)
+    indptr = torch.zeros(batch + 1, dtype=torch.int64)
+    indptr[1:] = torch.cumsum(lens, 0)
+    return DenseInputs(
+        batch=batch, q_len=q_len, num_heads=num_heads,
+        q_lat=q_lat, q_pe=q_pe, pool=pool,
+        seq_lens=lens.to(torch.int32), kv_indices=perm.contiguous(),
+        kv_indptr=indptr.to(torch.int32),
+        scale=float((d_v + d_rope) ** -0.5 if scale is None else scale),
+        kv_scale=float(kv_scale))
+
+
+def variable_lengths(batch: int, lo: int, hi: int, seed: int) -> torch.Tensor:
+    """Per-request lengths drawn uniformly from [lo, hi] (inclusive)."""
+    return torch.randint(lo, hi + 1, (batch,), generator=_gen(seed),
+                         dtype=torch.int64)
+
+
+def sparse_inputs(num_tokens: int, num_heads: int, topk: int, pool_rows: int,
+                  seed: int = 0, *, d_v: int = SPARSE_D_NOPE, d_rope: int = D_ROPE,
+                  kv_scale: float = KV_SCALE, scale: Optional[float] = None,
+                  invalid_frac: float = 0.0) -> SparseInputs:
+    """Sparse top-k inputs: per token ``topk`` distinct slots drawn without
+    replacement; with ``invalid_frac`` > 0 that fraction of entries is set to -1."""
+    g = _gen(seed)
+    q_nope = _bf16_normal((num_tokens, num_heads, d_v), g)
+    q_pe = _bf16_normal((num_tokens, num_heads, d_rope), g)
+    pool = fp8_pool(pool_rows, d_v + d_rope, g, kv_scale)
+    idx = torch.empty(num_tokens, topk, dtype=torch.int32)
+    for t in range(num_tokens):
+        idx[t] = torch.randperm(pool_rows, generator=g)[:topk].to(torch.int32)
+    if invalid_frac > 0:
+        mask = torch.rand(num_tokens, topk, generator=g) < invalid_frac
+        idx[mask] = -1
+    return SparseInputs(
+        num_tokens=num_tokens, num_heads=num_heads, topk=topk,
+        q_nope=q_nope, q_pe=q_pe, pool=pool, indices=idx,
+        scale=float((d_v + d_rope) ** -0.5 if scale is None else scale),
+        kv_scale=float(kv_scale))
+
+
+# --- the five synthetic workloads -------------------------------------------
+
+def workload_c0(seed: int = 0) -> DenseInputs:
+    """B=1, H=16, q_len=1, S=256."""
+    return dense_inputs(1, 1, 16, [256], seed)
+
+
+def workload_c1(q_len: int = 1, seed: int = 0, seq: int = 8192,
+                batch: int = 8) -> DenseInputs:
+    """B=8, H=16, S=8192 per request, q_len 1 or 4."""
+    return dense_inputs(batch, q_len, 16, [seq] * batch, seed)
+
+
+def workload_c2(batch: int, seq: int, seed: int = 0) -> DenseInputs:
+    """H=64, q_len=1, split-heavy (B, S) points."""
+    return dense_inputs(batch, 1, 64, [seq] * batch, seed)
+
+
+def workload_c3(seed: int = 0, batch: int = 64, lo: int = 1024,
+                hi: int = 32768) -> DenseInputs:
+    """B=64, H=128, q_len=1, lengths uniform in [1024, 32768]."""
+    lens = variable_lengths(batch, lo, hi, seed + 1000)
+    return dense_inputs(batch, 1, 128, lens, seed)
+
+
+def workload_c4(num_tokens: int, seed: int = 0, pool_rows: int = 131072,
+                topk: int = 2048) -> SparseInputs:
+    """Sparse top-k: T tokens, 64 heads, 448+64 dims, top-k 2048 of 131072."""
+    return sparse_inputs(num_tokens, 64, topk, pool_rows, seed)

@@ -1,0 +1,548 @@
+#!/usr/bin/env python3
+"""Benchmark: split-KV absorbed-MLA decode over a paged fp8 KV cache on GB300.
+
+A step is one full pass of the decode path (plan, split kernel over the paged
+fp8 rows, online base-2 softmax partials, split-K reduce) over one batch of the
+synthetic workload.  Default workload: B=8 requests, H=16 heads, S=8192 keys
+each, q_len=1, 576-byte e4m3fn rows (37.7 MB of KV per call).
+
+Timing: steps are captured into CUDA graphs (the pages' own method: "timed as
+CUDA-graph replays") and replayed; the inputs are rotated over enough device
+copies that the rotation is > 4x the L2 size, so every step streams its KV from
+HBM.  The dominant kernel's duration comes from CUDA events recorded around
+each of its launches on its own stream.  `e2e` repeats the measurement through
+the public call with host buffers: per step the queries and page table go
+host->device from pinned memory and o/lse come back.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle on
+the host's cores on the same metric instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MLA decode µs/call and achieved KV-stream HBM GB/s "
+          "(fraction of GB300 peak)")
+FALLBACK_HBM_GBS = 6800.0
+ROW_BYTES = {"dense": 576, "sparse": 512}
+
+
+# ---- workloads ------------------------------------------------------------------
+
+def make_workload(name: str):
+    from split_kv_mla_gb300 import inputs as gen
+    if name == "c0":
+        return "dense", gen.workload_c0(), "B=1 H=16 q_len=1 S=256"
+    if name in ("c1", "c1q1"):
+        return "dense", gen.workload_c1(q_len=1), "B=8 H=16 q_len=1 S=8192"
+    if name == "c1q4":
+        return "dense", gen.workload_c1(q_len=4), "B=8 H=16 q_len=4 S=8192"
+    if name.startswith("c2-"):
+        b, s = name[3:].split("x")
+        return "dense", gen.workload_c2(int(b), int(s)), f"B={b} H=64 q_len=1 S={s}"
+    if name == "c3":
+        return "dense", gen.workload_c3(), "B=64 H=128 q_len=1 S~U[1024,32768]"
+    if name.startswith("c4-"):
+        t = int(name[3:])
+        return "sparse", gen.workload_c4(t), f"T={t} H=64 top-k 2048 of 131072, 448+64"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def keys_per_call(kind, inp) -> int:
+    if kind == "dense":
+        return int(inp.seq_lens.sum())
+    return int((inp.indices >= 0).sum())
+
+
+def kv_bytes_per_call(kind, inp) -> int:
+    return keys_per_call(kind, inp) * ROW_BYTES[kind]
+
+
+def flops_per_call(kind, inp) -> int:
+    # 2 * (QK width + V width) per key and query row
+    if kind == "dense":
+        rows = inp.q_len * inp.num_heads
+        return 2 * (576 + 512) * rows * keys_per_call(kind, inp)
+    return 2 * (512 + 448) * inp.num_heads * keys_per_call(kind, inp)
+
+
+# ---- measured peaks, clocks, traffic ----------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.idx = device_id
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1", "0x1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def split_kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "split_kv_mla_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("mla_split") or f.endswith(".cuh"):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    or None if it was taken on another build of the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))
+        e = d[workload]
+        if e.get("kernel_src_sha") != split_kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---- our arm ---------------------------------------------------------------------
+
+class Runner:
+    """Device copies of one workload and the calls that run it."""
+
+    def __init__(self, kind, inp, device, copies):
+        from split_kv_mla_gb300 import mla
+        self.mla = mla
+        self.kind, self.inp, self.device = kind, inp, device
+        sms = mla.sm_count(device)
+        if kind == "dense":
+            self.plan = mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads,
+                                            inp.total_keys, sms)
+            base = dict(q_lat=inp.q_lat, q_pe=inp.q_pe, pool=inp.pool, seq_lens=inp.seq_lens,
+                        kv_indices=inp.kv_indices, kv_indptr=inp.kv_indptr)
+            rows = inp.batch * inp.q_len
+            self.o = torch.empty(rows, inp.num_heads, 512, dtype=torch.bfloat16, device=device)
+            self.lse = torch.empty(rows, inp.num_heads, dtype=torch.float32, device=device)
+        else:
+            self.plan = mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, sms)
+            base = dict(q_nope=inp.q_nope, q_pe=inp.q_pe, pool=inp.pool, indices=inp.indices)
+            self.o = torch.empty(inp.num_tokens, inp.num_heads, 448, dtype=torch.bfloat16,
+                                 device=device)
+            self.lse = torch.empty(inp.num_tokens, inp.num_heads, dtype=torch.float32,
+                                   device=device)
+        first = {k: v.to(device) for k, v in base.items()}
+        self.copies = [first] + [{k: v.clone() for k, v in first.items()}
+                                 for _ in range(copies - 1)]
+        self.ws = mla.workspace(self.plan, device)
+        self.sms = sms
+
+    def plan_step(self):
+        mla, inp = self.mla, self.inp
+        if self.kind == "dense":
+            return mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads, inp.total_keys,
+                                       self.sms)
+        return mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, self.sms)
+
+    def step(self, i, stream, splits_only=False, plan=None):
+        mla, inp, d = self.mla, self.inp, self.copies[i % len(self.copies)]
+        plan = plan or self.plan_step()
+        if self.kind == "dense":
+            fn = mla.mla_decode_splits if splits_only else mla.mla_decode
+            fn(plan, d["q_lat"], d["q_pe"], d["pool"], d["seq_lens"], d["kv_indices"],
+               d["kv_indptr"], inp.scale, inp.kv_scale, o_lat=self.o, lse=self.lse,
+               workspace_t=self.ws, stream=stream)
+        else:
+            fn = mla.mla_sparse_decode_splits if splits_only else mla.mla_sparse_decode
+            fn(plan, d["q_nope"], d["q_pe"], d["pool"], d["indices"], inp.scale, inp.kv_scale,
+               o=self.o, lse=self.lse, workspace_t=self.ws, stream=stream)
+
+    def reduce(self, stream):
+        o_part, lse_part = self.mla.mla_workspace_partials(self.plan, self.ws)
+        if o_part is None:
+            return
+        self.mla.mla_splitk_reduce(o_part, lse_part, self.inp.kv_scale,
+                                   o=self.o.view(-1, self.o.shape[-1]),
+                                   lse=self.lse.view(-1), stream=stream)
+
+    def launches_per_step(self):
+        return 1 + (1 if self.plan.num_splits > 1 else 0)
+
+    def copy_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.copies[0].values())
+
+
+def capture(runner, stream, n, offset=0):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                runner.step(offset + i, stream)
+    return g
+
+
+def time_steps(runner, stream, steps, copies):
+    """Device time of exactly `steps` steps (graph replays), in ms."""
+    full, rem = divmod(steps, copies)
+    g_full = capture(runner, stream, copies) if full else None
+    g_rem = capture(runner, stream, rem) if rem else None
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    return g_full, g_rem, full, start, end
+
+
+def kernel_times(runner, stream, n):
+    """Average device duration (ms) of the split kernel and the reduce kernel,
+    from events recorded around each launch on the launching stream."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    plan = runner.plan
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(50_000_000)  # let the host enqueue ahead of the device
+        for i in range(n):
+            evs[i][0].record(stream)
+            runner.step(i, stream, splits_only=True, plan=plan)
+            evs[i][1].record(stream)
+            runner.reduce(stream)
+            evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    split = [e[0].elapsed_time(e[1]) for e in evs]
+    red = [e[1].elapsed_time(e[2]) for e in evs]
+    return statistics.mean(split), statistics.mean(red)
+
+
+def e2e_measure(runner, stream, steps):
+    """Same metric through the public call with host buffers: H2D of queries and
+    page table from pinned memory, decode, D2H of o and lse, every step."""
+    inp = runner.inp
+    if runner.kind == "dense":
+        host = dict(q_lat=inp.q_lat, q_pe=inp.q_pe, seq_lens=inp.seq_lens,
+                    kv_indices=inp.kv_indices, kv_indptr=inp.kv_indptr)
+    else:
+        host = dict(q_nope=inp.q_nope, q_pe=inp.q_pe, indices=inp.indices)
+    host = {k: v.contiguous().pin_memory() for k, v in host.items()}
+    dev = runner.copies[0]
+    o_host = torch.empty(runner.o.shape, dtype=runner.o.dtype).pin_memory()
+    l_host = torch.empty(runner.lse.shape, dtype=runner.lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o_host.numel() * o_host.element_size() + l_host.numel() * l_host.element_size()
+
+    def one():
+        for k, v in host.items():
+            dev[k].copy_(v, non_blocking=True)
+        runner.step(0, stream)
+        o_host.copy_(runner.o, non_blocking=True)
+        l_host.copy_(runner.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            one()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def cpu_baseline(kind, inp, budget_s: float):
+    """fp64 oracle on the host's cores over a bounded sample of the workload:
+    whole requests (all heads and draft rows), repeated until about budget_s."""
+    from oracle import oracle
+    oracle.build()
+    if kind == "dense":
+        n_req = inp.batch
+        req_keys = inp.seq_lens.tolist()
+        heads_rows = inp.q_len * inp.num_heads
+    else:
+        n_req = inp.num_tokens
+        req_keys = (inp.indices >= 0).sum(1).tolist()
+        heads_rows = inp.num_heads
+    # time one request, then size the sample
+    t0 = time.perf_counter()
+    items = list(range(0, heads_rows))
+    _oracle_items(kind, inp, items)
+    t1 = time.perf_counter() - t0
+    per_req = max(t1, 1e-4)
+    n = max(1, min(n_req, int(budget_s / per_req)))
+    items = list(range(0, n * heads_rows))
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _oracle_items(kind, inp, items)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s * 0.5 or reps >= 50:
+            break
+    keys = sum(req_keys[:n]) * reps
+    gbs = keys * ROW_BYTES[kind] / el / 1e9
+    sample = (f"{n} of {n_req} {'requests' if kind == 'dense' else 'tokens'} "
+              f"(all {heads_rows} rows each), {reps} pass(es), {el:.1f} s")
+    return {"value": gbs, "unit": "GB/s", "cores": oracle.cpu_threads(), "kind": "oracle",
+            "sample": sample}
+
+
+def _oracle_items(kind, inp, items):
+    import numpy as np
+    from oracle import oracle
+    sel = np.asarray(items, dtype=np.int64)
+    if kind == "dense":
+        oracle.dense_decode(inp, sel)
+    else:
+        oracle.sparse_decode(inp, sel)
+
+
+def run_ours(args, rank, world, local_rank):
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    from split_kv_mla_gb300 import mla
+    mla.load()
+    kind, inp, desc = make_workload(args.workload)
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
+    # rotation copies: total input bytes > 4x L2
+    from split_kv_mla_gb300 import mla as _m  # noqa: F401
+    per_copy = (inp.pool.numel() + (inp.q_lat.numel() * 2 if kind == "dense" else inp.q_nope.numel() * 2)
+                + inp.q_pe.numel() * 2 + (inp.kv_indices.numel() * 4 if kind == "dense"
+                                          else inp.indices.numel() * 4))
+    copies = max(1, min(64, math.ceil(4 * l2 / max(per_copy, 1))))
+    runner = Runner(kind, inp, device, copies)
+    stream = torch.cuda.Stream(device)
+
+    # warm-up (eager) then graphs
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            runner.step(i, stream)
+    torch.cuda.synchronize()
+    g_full, g_rem, full, start, end = time_steps(runner, stream, args.steps, copies)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):  # warm the graphs too
+            if g_full is not None:
+                g_full.replay()
+                break
+    torch.cuda.synchronize()
+
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else
+                           (uuid or str(local_rank)))
+    sampler.start()
+    time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = start.elapsed_time(end)
+    # keep the device busy until the sampler has seen load
+    t_load = time.perf_counter()
+    while ms_total < 1500 and time.perf_counter() - t_load < 1.5 and g_full is not None:
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                g_full.replay()
+        torch.cuda.synchronize()
+    sampler.stop()
+    clocks = sampler.summary()
+
+    if world > 1:
+        t = torch.tensor([ms_total], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    bytes_call = kv_bytes_per_call(kind, inp)
+    value = bytes_call * world / (ms_step * 1e-3) / 1e9
+
+    split_ms, reduce_ms = kernel_times(runner, stream, min(200, max(20, args.steps)))
+    e2e_ms, h2d, d2h = e2e_measure(runner, stream, min(200, max(20, args.steps)))
+    peak, peak_src = measured_peaks()
+    achieved = bytes_call / (split_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+
+    if rank != 0:
+        return None
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3fn-kv/bf16-q/fp32-acc",
+        "data": "synthetic (seeded; N(0,1) bf16 queries, N(0,1)/kv_scale e4m3fn pool, shuffled page_size-1 slots)",
+        "config": {"workload": f"{args.workload}: dense MLA decode {desc}" if kind == "dense"
+                   else f"{args.workload}: sparse top-k MLA decode {desc}",
+                   "kv_bytes_per_call": bytes_call, "keys_per_call": keys_per_call(kind, inp),
+                   "num_splits": runner.plan.num_splits, "head_blocks": runner.plan.head_blocks,
+                   "l2": f"inputs rotated over {copies} device copies "
+                         f"({copies * per_copy / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA-graph replays, CUDA events on the launch stream",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": ms_step * 1e3,
+        "keys_per_s": keys_per_call(kind, inp) * world / (ms_step * 1e-3),
+        "hbm_frac_of_measured": round(value / world / peak, 4),
+        "gpu_launches": args.steps * runner.launches_per_step(),
+        "kernels": {"split_ms": split_ms, "reduce_ms": reduce_ms,
+                    "split_share": split_ms / (split_ms + reduce_ms) if reduce_ms > 0 else 1.0},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": peak_src, "kernel": "split kernel",
+                     "algorithmic_bytes": bytes_call},
+        "e2e": {"value": round(bytes_call / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+        "tflops": flops_per_call(kind, inp) / (ms_step * 1e-3) / 1e12,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(kind, inp, args.cpu_budget)
+    return out
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host's cores, same workload and metric."""
+    if rank != 0:
+        return None
+    from oracle import oracle
+    oracle.build()
+    kind, inp, desc = make_workload(args.workload)
+    # one step = a bounded sample: the first request (all rows), fixed across steps
+    if kind == "dense":
+        heads_rows = inp.q_len * inp.num_heads
+        n_req = max(1, min(inp.batch, args.ref_requests))
+        keys = int(inp.seq_lens[:n_req].sum())
+    else:
+        heads_rows = inp.num_heads
+        n_req = max(1, min(inp.num_tokens, args.ref_requests))
+        keys = int((inp.indices[:n_req] >= 0).sum())
+    items = list(range(n_req * heads_rows))
+    for _ in range(args.warmup):
+        _oracle_items(kind, inp, items)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_items(kind, inp, items)
+    el = time.perf_counter() - t0
+    ms_step = el / args.steps * 1e3
+    value = keys * ROW_BYTES[kind] / (ms_step * 1e-3) / 1e9
+    sample = (f"{n_req} {'request' if kind == 'dense' else 'token'}(s) of the workload, "
+              f"all {heads_rows} rows, per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, same recipe as the GPU arm)",
+        "config": {"workload": f"{args.workload}: {desc}", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.cpu_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c1q1")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-requests", type=int, default=1)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

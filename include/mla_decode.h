@@ -1,0 +1,246 @@
+/*
+ * mla_decode.h -- C ABI of libmla: split-KV absorbed-MLA decode over a paged
+ * fp8 e4m3fn KV cache on GB300 (sm_103a).
+ *
+ * The operation (moonmath-ai/amd-kernels README, "MLA absorbed decode",
+ * "Use / MLA decode" and "Constraints / MLA decode"):
+ *   one fused fp8 row per cached token is both K (all d_v + d_rope columns) and
+ *   V (the first d_v columns), dequantized by ONE per-tensor kv_scale; queries
+ *   come split into a latent part q_lat and a RoPE part q_pe; the pool is paged
+ *   with page_size 1, so kv_indices is a flat per-token slot list in which any
+ *   permutation or subset of the pool is legal; a call serves plain decode
+ *   (q_len 1) and speculative verify (q_len > 1: draft position t of a request of
+ *   S keys attends KV positions [0, S - q_len + t], inclusive); the output is
+ *   written in place and an optional base-2 log-sum-exp is returned.
+ *
+ * For query row r = b*q_len + t and head h, with k_j the dequantized rows of
+ * request b's visible positions:
+ *   s_j  = scale * (q_lat[r,h,:] . k_j[0:d_v] + q_pe[r,h,:] . k_j[d_v:d_v+d_rope])
+ *   o    = sum_j softmax(s)_j k_j[0:d_v]                    (bf16, round to nearest)
+ *   lse  = log2 sum_j 2^(s_j * log2 e)                        (fp32, base 2)
+ * A row that sees no key gets o = 0 and lse = -inf.
+ *
+ * Split-KV ("flash-decoding"): the planner splits each request's positions into
+ * num_splits contiguous ranges (hip_mha_decoding_num_partitions: wave-aligned
+ * split-K target, MLA-style branch); each (request, head block, split) CTA
+ * writes a normalized fp32 partial and its base-2 LSE to the workspace and a
+ * split-K reduce merges them in increasing split order, a fixed association
+ * (README, "Numerics": the merge sums in a fixed association, so results are
+ * deterministic run to run).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named q_*, pool, *indices, *indptr, seq_lens, o*, lse*, workspace
+ *     are DEVICE pointers owned by the caller; the library never allocates,
+ *     frees or keeps them past the call.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work on it: no host synchronisation, no allocation, so a call
+ *     can be captured into a CUDA graph (the plan depends on shapes alone).
+ *   - Return value: MLA_OK (0) or a negative MLA_ERR_* status; nothing is
+ *     enqueued when a status other than MLA_OK or MLA_ERR_LAUNCH_FAILED is
+ *     returned.  mla_status_string() names each status.
+ *   - Faults found on the device (a slot outside [0, pool_rows), a bounded wait
+ *     that ran out) are never raised as GPU faults: the kernel skips the bad
+ *     access, ORs an MLA_DEVERR_* bit into the workspace's error word and
+ *     finishes; outputs of the affected rows are then unspecified.  The word
+ *     is sticky: clear it with mla_workspace_reset() and read it with
+ *     mla_read_device_error().
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------- */
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARG (-1)         /* null pointer, negative size, plan/shape mismatch */
+#define MLA_ERR_UNSUPPORTED_SHAPE (-2)   /* d_v/d_rope not (512,64) dense or (448,64) sparse,
+                                            heads outside [1,128], too many splits */
+#define MLA_ERR_MISALIGNED (-3)          /* a buffer is not 16-byte aligned */
+#define MLA_ERR_WORKSPACE_TOO_SMALL (-4) /* workspace_bytes < plan->workspace_bytes */
+#define MLA_ERR_UNSUPPORTED_DEVICE (-5)  /* current device is not compute capability 10.3 */
+#define MLA_ERR_LAUNCH_FAILED (-6)       /* a kernel launch returned a CUDA error */
+#define MLA_ERR_CUDA (-7)                /* another CUDA runtime/driver call failed */
+
+/* ---- device error bits (workspace error word) ------------------------------- */
+#define MLA_DEVERR_BAD_SLOT 1u       /* a dense slot outside [0, pool_rows): key skipped */
+#define MLA_DEVERR_TIMEOUT 2u        /* a bounded pipeline wait ran out: CTA gave up */
+#define MLA_DEVERR_BAD_LENGTH 4u     /* seq_lens[b] outside [0, kv_indptr[b+1]-kv_indptr[b]] */
+
+/* Largest split count the reducer accepts (hip_mha_decoding_num_partitions: the
+ * reducer's 256-partition specialization caps the MLA-style split count). */
+#define MLA_MAX_SPLITS 256
+/* Bytes at the start of every workspace that hold the device error word. */
+#define MLA_WORKSPACE_HEADER_BYTES 256
+
+/*
+ * A launch plan: a pure function of shapes and the SM count (README, "MLA
+ * absorbed decode": the op plans from tensor shapes alone, so it is CUDA-graph
+ * capturable with no host synchronisation).  Plain data: copy it, store it,
+ * recompute it; it holds no pointer.  Fields after `variant` echo the shape the
+ * plan was made for; the decode entry points reject a plan whose echo differs
+ * from their arguments.
+ */
+typedef struct {
+    int32_t num_splits;      /* KV ranges per request (1..MLA_MAX_SPLITS) */
+    int32_t rows_per_cta;    /* query rows (draft position x head) per CTA */
+    int32_t block_n;         /* keys per pipeline block */
+    int32_t head_blocks;     /* CTAs sharing one (request, split) */
+    int32_t grid_x, grid_y, grid_z;  /* head_blocks, num_splits, batch (or tokens) */
+    int32_t variant;         /* kernel variant chosen for the shape */
+    int64_t workspace_bytes; /* bytes of device workspace the call needs */
+    int32_t batch, q_len, num_heads, d_v, d_rope, sm_count;
+    int64_t total_keys;      /* dense: kv_indices length; sparse: tokens * topk */
+} mla_plan_t;
+
+/*
+ * Dense plan.  total_keys = number of entries of kv_indices (a shape, not a
+ * value); sm_count = the device's multiProcessorCount.  d_v must be 512 and
+ * d_rope 64 (README, "Constraints / MLA decode": kv_lora_rank 512,
+ * qk_rope_head_dim 64); num_heads in [1, 128] (same passage: H 1..128); any
+ * q_len >= 1.  Writes *out and returns MLA_OK, or a status.
+ */
+int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t total_keys,
+                    int32_t d_v, int32_t d_rope, int32_t sm_count, mla_plan_t* out);
+
+/*
+ * Sparse top-k plan (flashinfer.mla.cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits:
+ * one decode call's (num_splits, chunks per CTA) from tokens, heads, top-k and
+ * the SM count; "[Perf] pa_decode_sparse ..." issue: 64 heads, 448 NoPE + 64
+ * RoPE columns, top-k 2048).  d_v must be 448 and d_rope 64.  max_splits bounds
+ * num_splits (0 = MLA_MAX_SPLITS); a bound below what the top-k needs is
+ * rejected with MLA_ERR_UNSUPPORTED_SHAPE (plan_splits raises likewise).
+ */
+int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
+                           int32_t d_v, int32_t d_rope, int32_t sm_count, int32_t max_splits,
+                           mla_plan_t* out);
+
+/*
+ * Dense decode: enqueues the split kernel and, when plan->num_splits > 1, the
+ * split-K reduce.  Layouts (row-major, contiguous):
+ *   q_lat    bf16 [batch*q_len, num_heads, 512]   row r = b*q_len + t
+ *   q_pe     bf16 [batch*q_len, num_heads, 64]
+ *   pool     e4m3fn bytes [pool_rows, 576] (a [pool_rows, 1, 576] tensor), 16-byte aligned
+ *   seq_lens int32 [batch]; kv_indptr int32 [batch+1]; kv_indices int32 [kv_indptr[batch]]
+ *            request b's position j lives in slot kv_indices[kv_indptr[b] + j],
+ *            j < seq_lens[b] <= kv_indptr[b+1] - kv_indptr[b]
+ *   o_lat    bf16 [batch*q_len, num_heads, 512], written
+ *   lse      fp32 [batch*q_len, num_heads] base 2, written when non-NULL
+ *   workspace >= plan->workspace_bytes bytes, 256-byte aligned; its first
+ *            MLA_WORKSPACE_HEADER_BYTES hold the error word, the rest is
+ *            scratch for the fp32 partials.  Calls that share a workspace must
+ *            not overlap on the GPU.
+ * scale multiplies the raw q.k dot product of dequantized rows (typically
+ * (512+64)^-0.5); kv_scale dequantizes the pool.
+ */
+int mla_decode(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+               const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+               const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+               int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+               void* o_lat, float* lse, void* workspace, int64_t workspace_bytes,
+               void* stream);
+
+/*
+ * Sparse top-k decode: token t attends the pool rows indices[t, 0:topk]
+ * (a negative entry is invalid and skipped, the has_invalid case of the
+ * pa_decode_sparse issue; a token with no valid entry gets o = 0, lse = -inf).
+ *   q_nope bf16 [num_tokens, num_heads, 448]; q_pe bf16 [num_tokens, num_heads, 64]
+ *   pool   e4m3fn bytes [pool_rows, 512]; indices int32 [num_tokens, topk]
+ *   o      bf16 [num_tokens, num_heads, 448]; lse fp32 [num_tokens, num_heads] or NULL
+ * Other arguments as for mla_decode.
+ */
+int mla_sparse_decode(const mla_plan_t* plan, const void* q_nope, const void* q_pe,
+                      const void* pool, int64_t pool_rows, const int32_t* indices,
+                      int32_t num_tokens, int32_t num_heads, int32_t topk, float scale,
+                      float kv_scale, void* o, float* lse, void* workspace,
+                      int64_t workspace_bytes, void* stream);
+
+/*
+ * The two halves of mla_decode / mla_sparse_decode, for callers that keep the
+ * per-split partials (for example to merge them with another rank's) or time
+ * the kernels one by one.  mla_decode_splits enqueues only the split kernel:
+ * with plan->num_splits == 1 it writes o_lat / lse exactly as mla_decode does;
+ * otherwise it leaves the normalized fp32 partials and their base-2 LSEs in the
+ * workspace, where mla_workspace_partials() finds them, and
+ * mla_splitk_reduce(o_part, lse_part, rows, num_splits, d_v, kv_scale, ...)
+ * finishes the call.  Arguments as for mla_decode / mla_sparse_decode.
+ */
+int mla_decode_splits(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+                      const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+                      const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+                      int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+                      void* o_lat, float* lse, void* workspace, int64_t workspace_bytes,
+                      void* stream);
+int mla_sparse_decode_splits(const mla_plan_t* plan, const void* q_nope, const void* q_pe,
+                             const void* pool, int64_t pool_rows, const int32_t* indices,
+                             int32_t num_tokens, int32_t num_heads, int32_t topk, float scale,
+                             float kv_scale, void* o, float* lse, void* workspace,
+                             int64_t workspace_bytes, void* stream);
+
+/*
+ * Device addresses, inside `workspace`, of the partials a plan's split kernel
+ * writes: o_part fp32 [rows, num_splits, d_v] and lse_part fp32
+ * [rows, num_splits], rows = batch * q_len * num_heads.  Host arithmetic only;
+ * both are NULL when plan->num_splits == 1.
+ */
+int mla_workspace_partials(const mla_plan_t* plan, void* workspace, float** o_part,
+                           float** lse_part);
+
+/*
+ * Split-K reduce on its own (hip_mha_decoding_num_partitions: the split-K
+ * reducer that merges up to 256 partitions).  For each of `rows` rows:
+ *   M = max_s lse_part[row, s];  w_s = 2^(lse_part[row, s] - M)
+ *   o[row, :]  = bf16(out_scale * sum_s w_s o_part[row, s, :] / sum_s w_s)
+ *   lse[row]   = M + log2 sum_s w_s            (when lse is non-NULL)
+ * with s in increasing order; a row whose partials are all -inf gets o = 0 and
+ * lse = -inf.  o_part fp32 [rows, num_splits, d_v] (normalized partials),
+ * lse_part fp32 [rows, num_splits] base 2, o bf16 [rows, d_v]; d_v a multiple
+ * of 8, num_splits in [1, MLA_MAX_SPLITS]; all 16-byte aligned.
+ */
+int mla_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
+                      int32_t num_splits, int32_t d_v, float out_scale, void* o,
+                      float* lse, void* stream);
+
+/*
+ * Re-target a plan to a forced split count (1..MLA_MAX_SPLITS), updating its
+ * grid and workspace size.  For split sweeps (moonmath-ai/amd-kernels README,
+ * "Results -- MLA decode": num_kv_splits swept per shape) and tests; the
+ * planner's own choice needs no call to it.
+ */
+int mla_plan_force_splits(mla_plan_t* plan, int32_t num_splits);
+
+/* Zero the workspace's error word (enqueued on `stream`). */
+int mla_workspace_reset(void* workspace, void* stream);
+
+/*
+ * Read the error word (MLA_DEVERR_* bits) into *code.  Synchronises `stream`;
+ * not for the hot path.
+ */
+int mla_read_device_error(const void* workspace, int32_t* code, void* stream);
+
+/* Static text for a status code. */
+const char* mla_status_string(int status);
+
+/*
+ * The split count that the wave-fill rule of hip_mha_decoding_num_partitions
+ * (MLA-style branch) gives for the given constants: ctas = ceil(heads/bm) *
+ * batch; one_wave = sm/ctas; two_wave = 2*sm/ctas; pages = ceil(keys/page);
+ * work_floor = ceil(pages/max_pages_per_split); np = clamp(work_floor,
+ * one_wave, two_wave) rounded up to a power of two, capped by two_wave, by
+ * max_splits and by pages; heads <= small_heads uses min(two_wave, pages).
+ * The dense planner calls it with GB300 constants; it is exported so the
+ * constants of the page it comes from can be checked against that page's
+ * printed sweep.
+ */
+int32_t mla_wave_fill_splits(int32_t batch, int64_t keys_per_request, int32_t heads,
+                             int32_t sm_count, int32_t bm, int32_t page,
+                             int32_t max_pages_per_split, int32_t max_splits,
+                             int32_t small_heads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DECODE_H */

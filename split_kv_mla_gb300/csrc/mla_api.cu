@@ -1,0 +1,419 @@
+// mla_api.cu -- the extern "C" boundary of libmla: planning, argument checks,
+// kernel dispatch and the workspace error word.  See include/mla_decode.h for
+// the contract of every entry point.
+#include <cmath>
+#include <cstring>
+
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kDenseDv = 512, kDenseDr = 64;
+constexpr int kSparseDv = 448, kSparseDr = 64;
+constexpr int kMaxHeads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Split-kernel geometry of the current variant.
+constexpr int kRowsPerCta = 16;
+constexpr int kBlockN = 32;
+
+// GB300 split rule constants (wave-fill, MLA-style branch of
+// hip_mha_decoding_num_partitions, re-derived for this kernel): the rule
+// targets `kWaves` resident waves of CTAs and at least kMinKeysPerSplit keys
+// per split; everything is a function of shapes and the SM count.
+constexpr int kWaves = 2;
+constexpr int kMinKeysPerSplit = 256;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+int device_ok()
+{
+    static int cached[64];  // 0 unknown, 1 ok, 2 not ok
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return MLA_ERR_UNSUPPORTED_DEVICE;
+    if (cached[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return MLA_ERR_CUDA;
+        cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return cached[dev] == 1 ? MLA_OK : MLA_ERR_UNSUPPORTED_DEVICE;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t workspace_for(int64_t items, int ns, int d_v)
+{
+    int64_t bytes = MLA_WORKSPACE_HEADER_BYTES;
+    if (ns > 1) {
+        bytes += align_up(items * ns * (int64_t)d_v * 4, 256);
+        bytes += align_up(items * ns * 4, 256);
+    }
+    return bytes;
+}
+
+// Split count for `ctas_per_split` CTAs per split and `keys` keys per request.
+int32_t gb300_splits(int64_t ctas_per_split, int64_t keys, int32_t sm_count)
+{
+    int64_t target = (int64_t)kWaves * sm_count / (ctas_per_split > 0 ? ctas_per_split : 1);
+    int64_t by_keys = ceil_div(keys > 0 ? keys : 1, kMinKeysPerSplit);
+    int64_t ns = target < by_keys ? target : by_keys;
+    if (ns < 1) ns = 1;
+    if (ns > MLA_MAX_SPLITS) ns = MLA_MAX_SPLITS;
+    return (int32_t)ns;
+}
+
+void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32_t d_v,
+               int32_t d_rope, int32_t sm_count, int64_t total_keys, int32_t ns)
+{
+    const int32_t rows = q_len * heads;
+    std::memset(p, 0, sizeof *p);
+    p->num_splits = ns;
+    p->rows_per_cta = kRowsPerCta;
+    p->block_n = kBlockN;
+    p->head_blocks = (int32_t)ceil_div(rows, kRowsPerCta);
+    p->grid_x = p->head_blocks;
+    p->grid_y = ns;
+    p->grid_z = batch;
+    p->variant = kVariantSimt;
+    p->workspace_bytes = workspace_for((int64_t)batch * rows, ns, d_v);
+    p->batch = batch;
+    p->q_len = q_len;
+    p->num_heads = heads;
+    p->d_v = d_v;
+    p->d_rope = d_rope;
+    p->sm_count = sm_count;
+    p->total_keys = total_keys;
+}
+
+int check_workspace(const mla_plan_t* plan, const void* ws, int64_t bytes)
+{
+    if (!ws) return MLA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MLA_ERR_MISALIGNED;
+    if (bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    return MLA_OK;
+}
+
+void carve(const mla_plan_t* plan, void* ws, int64_t items, SplitArgs* a)
+{
+    char* base = static_cast<char*>(ws);
+    a->err = reinterpret_cast<uint32_t*>(base);
+    if (plan->num_splits > 1) {
+        const int64_t obytes = align_up(items * plan->num_splits * (int64_t)plan->d_v * 4, 256);
+        a->o_part = reinterpret_cast<float*>(base + MLA_WORKSPACE_HEADER_BYTES);
+        a->lse_part = reinterpret_cast<float*>(base + MLA_WORKSPACE_HEADER_BYTES + obytes);
+    } else {
+        a->o_part = nullptr;
+        a->lse_part = nullptr;
+    }
+}
+
+int run(const mla_plan_t* plan, SplitArgs& a, int64_t items, cudaStream_t stream,
+        bool with_reduce)
+{
+    cudaError_t e = launch_split_simt(a, *plan, stream);
+    if (e != cudaSuccess) return MLA_ERR_LAUNCH_FAILED;
+    if (with_reduce && plan->num_splits > 1) {
+        e = launch_splitk_reduce(a.o_part, a.lse_part, items, plan->num_splits, plan->d_v,
+                                 a.out_scale, a.o, a.lse, stream);
+        if (e != cudaSuccess) return MLA_ERR_LAUNCH_FAILED;
+    }
+    return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int32_t mla_wave_fill_splits(int32_t batch, int64_t keys_per_request, int32_t heads,
+                             int32_t sm_count, int32_t bm, int32_t page,
+                             int32_t max_pages_per_split, int32_t max_splits,
+                             int32_t small_heads)
+{
+    if (batch <= 0 || heads <= 0 || sm_count <= 0 || bm <= 0 || page <= 0 ||
+        max_pages_per_split <= 0 || max_splits <= 0)
+        return 1;
+    const int64_t ctas = ceil_div(heads, bm) * batch;
+    const int64_t one_wave = sm_count / ctas;
+    const int64_t two_wave = 2LL * sm_count / ctas;
+    const int64_t pages = ceil_div(keys_per_request > 0 ? keys_per_request : 1, page);
+    int64_t np;
+    if (heads <= small_heads) {
+        np = two_wave < pages ? two_wave : pages;
+    } else {
+        const int64_t work_floor = ceil_div(pages, max_pages_per_split);
+        np = work_floor < one_wave ? one_wave : work_floor;
+        if (np > two_wave) np = two_wave;
+        int64_t p2 = 1;
+        while (p2 < np) p2 <<= 1;
+        np = p2 < two_wave ? p2 : two_wave;
+    }
+    if (np > max_splits) np = max_splits;
+    if (np > pages) np = pages;
+    if (np < 1) np = 1;
+    return (int32_t)np;
+}
+
+int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t total_keys,
+                    int32_t d_v, int32_t d_rope, int32_t sm_count, mla_plan_t* out)
+{
+    if (!out || batch < 0 || q_len < 1 || total_keys < 0 || sm_count < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (d_v != kDenseDv || d_rope != kDenseDr || num_heads < 1 || num_heads > kMaxHeads)
+        return MLA_ERR_UNSUPPORTED_SHAPE;
+    const int64_t rows = (int64_t)q_len * num_heads;
+    if (rows > (1 << 20)) return MLA_ERR_UNSUPPORTED_SHAPE;
+    const int64_t head_blocks = ceil_div(rows, kRowsPerCta);
+    const int64_t keys = batch > 0 ? ceil_div(total_keys, batch) : 0;
+    const int32_t ns = gb300_splits(head_blocks * (batch > 0 ? batch : 1), keys, sm_count);
+    fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ns);
+    return MLA_OK;
+}
+
+int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk, int32_t d_v,
+                           int32_t d_rope, int32_t sm_count, int32_t max_splits,
+                           mla_plan_t* out)
+{
+    if (!out || num_tokens < 0 || topk < 0 || sm_count < 1 || max_splits < 0)
+        return MLA_ERR_INVALID_ARG;
+    if (d_v != kSparseDv || d_rope != kSparseDr || num_heads < 1 || num_heads > kMaxHeads)
+        return MLA_ERR_UNSUPPORTED_SHAPE;
+    const int32_t cap = max_splits == 0 ? MLA_MAX_SPLITS
+                                        : (max_splits < MLA_MAX_SPLITS ? max_splits : MLA_MAX_SPLITS);
+    const int64_t head_blocks = ceil_div(num_heads, kRowsPerCta);
+    int32_t ns = gb300_splits(head_blocks * (num_tokens > 0 ? num_tokens : 1), topk, sm_count);
+    if (ns > cap) ns = cap;
+    fill_plan(out, num_tokens, 1, num_heads, d_v, d_rope, sm_count,
+              (int64_t)num_tokens * topk, ns);
+    return MLA_OK;
+}
+
+static int dense_call(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+                      const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+                      const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+                      int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+                      void* o_lat, float* lse, void* workspace, int64_t workspace_bytes,
+                      void* stream, bool with_reduce)
+{
+    if (!plan) return MLA_ERR_INVALID_ARG;
+    if (plan->batch != batch || plan->q_len != q_len || plan->num_heads != num_heads ||
+        plan->d_v != kDenseDv || plan->d_rope != kDenseDr || plan->variant != kVariantSimt ||
+        plan->num_splits < 1 || plan->num_splits > MLA_MAX_SPLITS)
+        return MLA_ERR_INVALID_ARG;
+    if (batch == 0) return MLA_OK;
+    if (!q_lat || !q_pe || !pool || !seq_lens || !kv_indptr || !o_lat || pool_rows < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (plan->total_keys > 0 && !kv_indices) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(pool) || !aligned16(o_lat))
+        return MLA_ERR_MISALIGNED;
+    if (!std::isfinite(scale) || !std::isfinite(kv_scale)) return MLA_ERR_INVALID_ARG;
+    int rc = check_workspace(plan, workspace, workspace_bytes);
+    if (rc != MLA_OK) return rc;
+    rc = device_ok();
+    if (rc != MLA_OK) return rc;
+
+    SplitArgs a{};
+    a.q_lat = static_cast<const uint16_t*>(q_lat);
+    a.q_pe = static_cast<const uint16_t*>(q_pe);
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.pool_rows = pool_rows;
+    a.seq_lens = seq_lens;
+    a.kv_indices = kv_indices;
+    a.kv_indptr = kv_indptr;
+    a.topk = 0;
+    a.batch = batch;
+    a.q_len = q_len;
+    a.num_heads = num_heads;
+    a.d_v = kDenseDv;
+    a.d_rope = kDenseDr;
+    a.num_splits = plan->num_splits;
+    a.rows_per_cta = plan->rows_per_cta;
+    a.head_blocks = plan->head_blocks;
+    a.logit_scale = scale * kv_scale * kLog2e;
+    a.out_scale = kv_scale;
+    a.o = static_cast<uint16_t*>(o_lat);
+    a.lse = lse;
+    a.sparse = 0;
+    const int64_t items = (int64_t)batch * q_len * num_heads;
+    carve(plan, workspace, items, &a);
+    return run(plan, a, items, static_cast<cudaStream_t>(stream), with_reduce);
+}
+
+static int sparse_call(const mla_plan_t* plan, const void* q_nope, const void* q_pe,
+                       const void* pool, int64_t pool_rows, const int32_t* indices,
+                       int32_t num_tokens, int32_t num_heads, int32_t topk, float scale,
+                       float kv_scale, void* o, float* lse, void* workspace,
+                       int64_t workspace_bytes, void* stream, bool with_reduce)
+{
+    if (!plan) return MLA_ERR_INVALID_ARG;
+    if (plan->batch != num_tokens || plan->q_len != 1 || plan->num_heads != num_heads ||
+        plan->d_v != kSparseDv || plan->d_rope != kSparseDr || plan->variant != kVariantSimt ||
+        plan->total_keys != (int64_t)num_tokens * topk || plan->num_splits < 1 ||
+        plan->num_splits > MLA_MAX_SPLITS)
+        return MLA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MLA_OK;
+    if (!q_nope || !q_pe || !pool || !o || pool_rows < 1 || topk < 0)
+        return MLA_ERR_INVALID_ARG;
+    if (topk > 0 && !indices) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(pool) || !aligned16(o))
+        return MLA_ERR_MISALIGNED;
+    if (!std::isfinite(scale) || !std::isfinite(kv_scale)) return MLA_ERR_INVALID_ARG;
+    int rc = check_workspace(plan, workspace, workspace_bytes);
+    if (rc != MLA_OK) return rc;
+    rc = device_ok();
+    if (rc != MLA_OK) return rc;
+
+    SplitArgs a{};
+    a.q_lat = static_cast<const uint16_t*>(q_nope);
+    a.q_pe = static_cast<const uint16_t*>(q_pe);
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.pool_rows = pool_rows;
+    a.seq_lens = nullptr;
+    a.kv_indices = indices;
+    a.kv_indptr = nullptr;
+    a.topk = topk;
+    a.batch = num_tokens;
+    a.q_len = 1;
+    a.num_heads = num_heads;
+    a.d_v = kSparseDv;
+    a.d_rope = kSparseDr;
+    a.num_splits = plan->num_splits;
+    a.rows_per_cta = plan->rows_per_cta;
+    a.head_blocks = plan->head_blocks;
+    a.logit_scale = scale * kv_scale * kLog2e;
+    a.out_scale = kv_scale;
+    a.o = static_cast<uint16_t*>(o);
+    a.lse = lse;
+    a.sparse = 1;
+    const int64_t items = (int64_t)num_tokens * num_heads;
+    carve(plan, workspace, items, &a);
+    return run(plan, a, items, static_cast<cudaStream_t>(stream), with_reduce);
+}
+
+int mla_decode(const mla_plan_t* plan, const void* q_lat, const void* q_pe, const void* pool,
+               int64_t pool_rows, const int32_t* seq_lens, const int32_t* kv_indices,
+               const int32_t* kv_indptr, int32_t batch, int32_t q_len, int32_t num_heads,
+               float scale, float kv_scale, void* o_lat, float* lse, void* workspace,
+               int64_t workspace_bytes, void* stream)
+{
+    return dense_call(plan, q_lat, q_pe, pool, pool_rows, seq_lens, kv_indices, kv_indptr,
+                      batch, q_len, num_heads, scale, kv_scale, o_lat, lse, workspace,
+                      workspace_bytes, stream, true);
+}
+
+int mla_decode_splits(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+                      const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+                      const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+                      int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+                      void* o_lat, float* lse, void* workspace, int64_t workspace_bytes,
+                      void* stream)
+{
+    return dense_call(plan, q_lat, q_pe, pool, pool_rows, seq_lens, kv_indices, kv_indptr,
+                      batch, q_len, num_heads, scale, kv_scale, o_lat, lse, workspace,
+                      workspace_bytes, stream, false);
+}
+
+int mla_sparse_decode(const mla_plan_t* plan, const void* q_nope, const void* q_pe,
+                      const void* pool, int64_t pool_rows, const int32_t* indices,
+                      int32_t num_tokens, int32_t num_heads, int32_t topk, float scale,
+                      float kv_scale, void* o, float* lse, void* workspace,
+                      int64_t workspace_bytes, void* stream)
+{
+    return sparse_call(plan, q_nope, q_pe, pool, pool_rows, indices, num_tokens, num_heads,
+                       topk, scale, kv_scale, o, lse, workspace, workspace_bytes, stream, true);
+}
+
+int mla_sparse_decode_splits(const mla_plan_t* plan, const void* q_nope, const void* q_pe,
+                             const void* pool, int64_t pool_rows, const int32_t* indices,
+                             int32_t num_tokens, int32_t num_heads, int32_t topk, float scale,
+                             float kv_scale, void* o, float* lse, void* workspace,
+                             int64_t workspace_bytes, void* stream)
+{
+    return sparse_call(plan, q_nope, q_pe, pool, pool_rows, indices, num_tokens, num_heads,
+                       topk, scale, kv_scale, o, lse, workspace, workspace_bytes, stream, false);
+}
+
+int mla_workspace_partials(const mla_plan_t* plan, void* workspace, float** o_part,
+                           float** lse_part)
+{
+    if (!plan || !workspace || !o_part || !lse_part) return MLA_ERR_INVALID_ARG;
+    SplitArgs a{};
+    carve(plan, workspace, (int64_t)plan->batch * plan->q_len * plan->num_heads, &a);
+    *o_part = a.o_part;
+    *lse_part = a.lse_part;
+    return MLA_OK;
+}
+
+int mla_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
+                      int32_t num_splits, int32_t d_v, float out_scale, void* o, float* lse,
+                      void* stream)
+{
+    if (rows < 0 || num_splits < 1 || num_splits > MLA_MAX_SPLITS || d_v < 8 || (d_v % 8) != 0 ||
+        d_v > 4 * 128)
+        return rows < 0 || num_splits < 1 ? MLA_ERR_INVALID_ARG : MLA_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MLA_OK;
+    if (!o_part || !lse_part || !o) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(o_part) || !aligned16(o)) return MLA_ERR_MISALIGNED;
+    if (!std::isfinite(out_scale)) return MLA_ERR_INVALID_ARG;
+    int rc = device_ok();
+    if (rc != MLA_OK) return rc;
+    cudaError_t e = launch_splitk_reduce(o_part, lse_part, rows, num_splits, d_v, out_scale,
+                                         static_cast<uint16_t*>(o), lse,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH_FAILED;
+}
+
+int mla_plan_force_splits(mla_plan_t* plan, int32_t num_splits)
+{
+    if (!plan || num_splits < 1 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+    if (plan->q_len < 1 || plan->num_heads < 1 || plan->batch < 0) return MLA_ERR_INVALID_ARG;
+    plan->num_splits = num_splits;
+    plan->grid_y = num_splits;
+    plan->workspace_bytes = workspace_for((int64_t)plan->batch * plan->q_len * plan->num_heads,
+                                          num_splits, plan->d_v);
+    return MLA_OK;
+}
+
+int mla_workspace_reset(void* workspace, void* stream)
+{
+    if (!workspace) return MLA_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t),
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_read_device_error(const void* workspace, int32_t* code, void* stream)
+{
+    if (!workspace || !code) return MLA_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+    *code = (int32_t)v;
+    return MLA_OK;
+}
+
+const char* mla_status_string(int status)
+{
+    switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MLA_ERR_MISALIGNED: return "buffer not 16-byte aligned (workspace: 256-byte)";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MLA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (need compute capability 10.3)";
+    case MLA_ERR_LAUNCH_FAILED: return "kernel launch failed";
+    case MLA_ERR_CUDA: return "CUDA runtime call failed";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

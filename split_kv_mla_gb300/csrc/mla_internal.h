@@ -1,0 +1,45 @@
+// mla_internal.h -- host-side declarations shared by the libmla translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+
+// Parameters of one split-kernel launch (dense or sparse).
+struct SplitArgs {
+    const uint16_t* q_lat;      // bf16 [rows, H, d_v]  (dense q_lat / sparse q_nope)
+    const uint16_t* q_pe;       // bf16 [rows, H, d_rope]
+    const uint8_t* pool;        // e4m3fn [pool_rows, d_v + d_rope]
+    int64_t pool_rows;
+    const int32_t* seq_lens;    // dense: [batch]; sparse: NULL (every token has topk entries)
+    const int32_t* kv_indices;  // dense: flat slot list; sparse: [tokens, topk]
+    const int32_t* kv_indptr;   // dense: [batch+1]; sparse: NULL (token t starts at t*topk)
+    int32_t topk;               // sparse only
+    int32_t batch;              // requests (dense) or tokens (sparse)
+    int32_t q_len;              // 1 for sparse
+    int32_t num_heads;
+    int32_t d_v, d_rope;
+    int32_t num_splits, rows_per_cta, head_blocks;
+    float logit_scale;          // scale * kv_scale * log2(e): raw fp8 dot -> base-2 logit
+    float out_scale;            // kv_scale: raw fp8 V units -> output units
+    uint16_t* o;                // bf16 [rows, H, d_v]   (written when num_splits == 1)
+    float* lse;                 // fp32 [rows, H] or NULL
+    float* o_part;              // fp32 [rows*H, ns, d_v] (num_splits > 1)
+    float* lse_part;            // fp32 [rows*H, ns]
+    uint32_t* err;              // workspace error word
+    int sparse;
+};
+
+// Kernel variants (mla_plan_t::variant).
+enum Variant : int32_t {
+    kVariantSimt = 1,   // CUDA-core split kernel
+};
+
+cudaError_t launch_split_simt(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
+                                 int32_t num_splits, int32_t d_v, float out_scale,
+                                 uint16_t* o, float* lse, cudaStream_t stream);
+
+}  // namespace mla

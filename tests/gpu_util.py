@@ -1,0 +1,68 @@
+"""Helpers for the GPU parity tests: move seeded inputs to the device, run the
+library, and compare against the fp64 oracle with the stated tolerances."""
+import numpy as np
+import torch
+
+from split_kv_mla_gb300 import mla
+
+# Parity bar for floating-point outputs: max-abs 1e-2 and relative RMS 5e-3 on
+# the attention output, 1e-3 absolute on the base-2 LSE.
+O_MAX_ABS = 1e-2
+O_REL_RMS = 5e-3
+LSE_ABS = 1e-3
+
+
+def dense_to_cuda(inp, device="cuda"):
+    return dict(
+        q_lat=inp.q_lat.to(device), q_pe=inp.q_pe.to(device), pool=inp.pool.to(device),
+        seq_lens=inp.seq_lens.to(device), kv_indices=inp.kv_indices.to(device),
+        kv_indptr=inp.kv_indptr.to(device))
+
+
+def run_dense(inp, plan=None, sms=None, device="cuda", ws=None):
+    d = dense_to_cuda(inp, device)
+    if plan is None:
+        plan = mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads, inp.total_keys,
+                                   sms or mla.sm_count())
+    o, lse = mla.mla_decode(plan, d["q_lat"], d["q_pe"], d["pool"], d["seq_lens"],
+                            d["kv_indices"], d["kv_indptr"], inp.scale, inp.kv_scale,
+                            workspace_t=ws)
+    torch.cuda.synchronize()
+    return o, lse, plan
+
+
+def run_sparse(inp, plan=None, device="cuda", max_splits=0, ws=None):
+    if plan is None:
+        plan = mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk,
+                                          mla.sm_count(), max_splits)
+    o, lse = mla.mla_sparse_decode(plan, inp.q_nope.to(device), inp.q_pe.to(device),
+                                   inp.pool.to(device), inp.indices.to(device), inp.scale,
+                                   inp.kv_scale, workspace_t=ws)
+    torch.cuda.synchronize()
+    return o, lse, plan
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    """Assert the parity bar; returns (max_abs, rel_rms, lse_max_abs)."""
+    o = o_gpu.float().cpu().double().numpy().reshape(o_ref.shape)
+    l = lse_gpu.float().cpu().double().numpy().reshape(lse_ref.shape)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    diff = o - o_ref
+    max_abs = float(np.max(np.abs(diff))) if diff.size else 0.0
+    denom = float(np.sqrt(np.mean(o_ref ** 2))) if o_ref.size else 0.0
+    rel_rms = float(np.sqrt(np.mean(diff ** 2)) / denom) if denom > 0 else float(
+        np.sqrt(np.mean(diff ** 2)) if diff.size else 0.0)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(l), fin), f"{what}: lse finiteness differs"
+    assert np.array_equal(l[~fin], lse_ref[~fin]), f"{what}: -inf rows differ"
+    lse_err = float(np.max(np.abs(l[fin] - lse_ref[fin]))) if fin.any() else 0.0
+    assert max_abs <= O_MAX_ABS, f"{what}: max-abs {max_abs}"
+    assert rel_rms <= O_REL_RMS, f"{what}: rel-RMS {rel_rms}"
+    assert lse_err <= LSE_ABS, f"{what}: lse err {lse_err}"
+    return max_abs, rel_rms, lse_err
+
+
+def sample_items(n_items, k, seed):
+    g = np.random.default_rng(seed)
+    pick = g.choice(n_items, size=min(k, n_items), replace=False)
+    return np.unique(np.concatenate([pick, [0, n_items - 1]]).astype(np.int64))

@@ -1,0 +1,158 @@
+"""Host-side checks of libmla that need no GPU: the library builds for sm_103a,
+loads, exports every entry point its header declares, plans from shapes alone,
+and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import shutil
+
+import pytest
+
+from split_kv_mla_gb300 import build as mla_build
+from split_kv_mla_gb300 import mla
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+needs_nvcc = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(mla_build.LIB):
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("library not built and nvcc not available")
+        mla_build.build()
+    import torch  # noqa: F401  (loads libcudart for the dynamic linker)
+    return mla.load()
+
+
+@needs_nvcc
+def test_build_is_up_to_date():
+    assert os.path.exists(mla_build.build())
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = mla.declared_symbols()
+    assert {"mla_decode_plan", "mla_decode", "mla_sparse_decode", "mla_splitk_reduce",
+            "mla_sparse_decode_plan"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(-7, 1):
+        s = mla.status_string(code)
+        assert s and s != "unknown status"
+    assert mla.status_string(-99) == "unknown status"
+
+
+def _golden_rows(name):
+    rows = []
+    for line in open(os.path.join(HERE, "golden", name)):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            rows.append([int(x) for x in line.split()])
+    return rows
+
+
+def test_wave_fill_rule_reproduces_printed_mi355x_sweep(lib):
+    # hip_mha_decoding_num_partitions, "Phase 0 sweep": MI355X constants
+    for batch, keys, heads, expected in _golden_rows("wave_fill_mi355x.txt"):
+        got = mla.mla_wave_fill_splits(batch, keys, heads, 256, 32, 256, 5, 256, 16)
+        assert got == expected, (batch, keys, heads, got, expected)
+
+
+def test_wave_fill_small_heads_exception(lib):
+    # num_heads <= 16: np = min(two_wave, pages)
+    assert mla.mla_wave_fill_splits(4, 32768, 16, 256, 32, 256, 5, 256, 16) == 128
+    assert mla.mla_wave_fill_splits(8, 1024, 16, 256, 32, 256, 5, 256, 16) == 4
+    # bs=1 two_wave = 512 clamps to the 256 cap
+    assert mla.mla_wave_fill_splits(1, 131072, 16, 256, 32, 256, 5, 256, 16) == 256
+
+
+@pytest.mark.parametrize("batch,q_len,heads,keys", [
+    (1, 1, 16, 256), (8, 1, 16, 8192 * 8), (8, 4, 16, 8192 * 8), (1, 1, 64, 131072),
+    (2, 1, 64, 131072), (8, 1, 64, 8 * 131072), (16, 1, 64, 16 * 131072),
+    (64, 1, 128, 1081344), (3, 7, 5, 10), (1, 1, 1, 0), (0, 1, 16, 0)])
+def test_dense_plan_invariants(lib, batch, q_len, heads, keys):
+    p = mla.mla_decode_plan(batch, q_len, heads, keys, 152)
+    assert 1 <= p.num_splits <= mla.MLA_MAX_SPLITS
+    assert p.head_blocks * p.rows_per_cta >= q_len * heads
+    assert (p.grid_x, p.grid_y, p.grid_z) == (p.head_blocks, p.num_splits, batch)
+    assert (p.batch, p.q_len, p.num_heads, p.d_v, p.d_rope, p.total_keys) == (
+        batch, q_len, heads, 512, 64, keys)
+    items = batch * q_len * heads
+    expect = 256
+    if p.num_splits > 1:
+        def up(x):
+            return -(-x // 256) * 256
+        expect += up(items * p.num_splits * 512 * 4) + up(items * p.num_splits * 4)
+    assert p.workspace_bytes == expect
+    # a plan is a pure function of its arguments
+    q = mla.mla_decode_plan(batch, q_len, heads, keys, 152)
+    assert p.as_dict() == q.as_dict()
+
+
+def test_force_splits_recomputes_grid_and_workspace(lib):
+    p = mla.mla_decode_plan(8, 1, 16, 8 * 8192, 152)
+    for ns in (1, 3, 256):
+        q = mla.mla_plan_force_splits(p, ns)
+        assert q.num_splits == ns and q.grid_y == ns
+        items = 8 * 16
+        up = lambda x: -(-x // 256) * 256  # noqa: E731
+        expect = 256 + ((up(items * ns * 512 * 4) + up(items * ns * 4)) if ns > 1 else 0)
+        assert q.workspace_bytes == expect
+    with pytest.raises(mla.MlaError):
+        mla.mla_plan_force_splits(p, 0)
+    with pytest.raises(mla.MlaError):
+        mla.mla_plan_force_splits(p, 257)
+
+
+def test_plan_rejections(lib):
+    with pytest.raises(mla.MlaError):
+        mla.mla_decode_plan(1, 1, 16, 10, 152, d_v=448)
+    with pytest.raises(mla.MlaError):
+        mla.mla_decode_plan(1, 1, 129, 10, 152)
+    with pytest.raises(mla.MlaError):
+        mla.mla_decode_plan(1, 1, 0, 10, 152)
+    with pytest.raises(mla.MlaError):
+        mla.mla_decode_plan(1, 0, 16, 10, 152)
+    with pytest.raises(mla.MlaError):
+        mla.mla_sparse_decode_plan(4, 64, 2048, 152, d_v=512)
+
+
+def test_sparse_plan_max_splits(lib):
+    p = mla.mla_sparse_decode_plan(1, 64, 2048, 152)
+    assert p.num_splits >= 1 and p.total_keys == 2048
+    q = mla.mla_sparse_decode_plan(1, 64, 2048, 152, max_splits=1)
+    assert q.num_splits == 1
+
+
+def _call_decode(lib, plan, ptr=0x10000, ws_bytes=1 << 20, batch=1, q_len=1, heads=16):
+    P = ctypes.c_void_p
+    return lib.mla_decode(ctypes.byref(plan) if plan is not None else None,
+                          P(ptr), P(ptr), P(ptr), 10, P(ptr), P(ptr), P(ptr), batch, q_len,
+                          heads, 0.1, 1.0, P(ptr), None, P(0x100000), ws_bytes, None)
+
+
+def test_decode_argument_checks_run_before_the_device(lib):
+    plan = mla.mla_decode_plan(1, 1, 16, 256, 152)
+    assert _call_decode(lib, None) == -1
+    assert _call_decode(lib, plan, heads=8) == -1          # plan/shape mismatch
+    assert _call_decode(lib, plan, ptr=0x10004) == -3      # misaligned
+    assert _call_decode(lib, plan, ws_bytes=16) == -4      # workspace too small
+    bad = mla.mla_decode_plan(1, 1, 16, 256, 152)
+    bad.num_splits = 0
+    assert _call_decode(lib, bad) == -1
+    # a zero-size batch is a no-op even without a device
+    empty = mla.mla_decode_plan(0, 1, 16, 0, 152)
+    assert _call_decode(lib, empty, batch=0) == 0
+
+
+def test_reduce_argument_checks(lib):
+    P = ctypes.c_void_p
+    assert lib.mla_splitk_reduce(P(0x1000), P(0x1000), 4, 0, 512, 1.0, P(0x1000), None, None) == -1
+    assert lib.mla_splitk_reduce(P(0x1000), P(0x1000), 4, 257, 512, 1.0, P(0x1000), None, None) == -2
+    assert lib.mla_splitk_reduce(P(0x1000), P(0x1000), 4, 2, 12, 1.0, P(0x1000), None, None) == -2
+    assert lib.mla_splitk_reduce(P(0x1004), P(0x1000), 4, 2, 512, 1.0, P(0x1000), None, None) == -3
+    assert lib.mla_splitk_reduce(None, None, 0, 2, 512, 1.0, None, None, None) == 0

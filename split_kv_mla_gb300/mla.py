@@ -181,6 +181,10 @@ def mla_decode(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv_ind
                scale: float, kv_scale: float, o_lat=None, lse=None, workspace_t=None,
                stream=None, return_lse: bool = True, _entry: str = "mla_decode"):
     """Dense decode; returns (o_lat, lse).  Outputs are allocated when not given."""
+    for name, t in (("q_lat", q_lat), ("q_pe", q_pe), ("pool", pool), ("seq_lens", seq_lens),
+                    ("kv_indices", kv_indices), ("kv_indptr", kv_indptr)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
     R, H = q_lat.shape[0], q_lat.shape[1]
     batch = seq_lens.shape[0]
     q_len = R // batch if batch else 1
@@ -211,6 +215,9 @@ def mla_sparse_decode(plan: mla_plan_t, q_nope, q_pe, pool, indices, scale: floa
                       kv_scale: float, o=None, lse=None, workspace_t=None, stream=None,
                       return_lse: bool = True, _entry: str = "mla_sparse_decode"):
     """Sparse top-k decode; returns (o, lse)."""
+    for name, t in (("q_nope", q_nope), ("q_pe", q_pe), ("pool", pool), ("indices", indices)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
     T, H = q_nope.shape[0], q_nope.shape[1]
     topk = indices.shape[1] if indices.dim() == 2 else 0
     if o is None:

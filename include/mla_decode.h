@@ -221,6 +221,36 @@ int mla_workspace_reset(void* workspace, void* stream);
  */
 int mla_read_device_error(const void* workspace, int32_t* code, void* stream);
 
+/*
+ * Dense decode for callers that cannot allocate device memory: code running
+ * where cudaMalloc is unavailable or not allowed (a no-allocation region of a
+ * serving loop with a fixed memory budget, or a host framework that hands over
+ * only its input and output buffers).  It is mla_decode with the workspace
+ * replaced by a static scratch array inside the library, so the caller passes
+ * inputs and outputs only and the call itself allocates nothing.  The pages
+ * have no counterpart of this entry point.
+ *   - Scratch: a file-scope __device__ array of MLA_NOALLOC_SCRATCH_BYTES; every
+ *     GPU that loads the library holds it until the process exits.  A plan with
+ *     plan->workspace_bytes above that size is rejected with
+ *     MLA_ERR_WORKSPACE_TOO_SMALL and nothing is enqueued.
+ *   - Set-up: the first call on a device (with that device current) looks up
+ *     the array's device address once; make that first call before any stream
+ *     capture on the device.
+ *   - Every call shares the one array and it keeps the last call's contents, so
+ *     calls that overlap on the GPU (on different streams, or from different
+ *     threads) race and must be serialised by the caller.
+ *   - Device-side error bits (MLA_DEVERR_*) are not reported by this entry
+ *     point: bad slots are still skipped safely, but there is no workspace to
+ *     read them from.
+ * Other arguments, layouts and status codes as for mla_decode.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)
+int mla_decode_noalloc(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+                       const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+                       const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+                       int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+                       void* o_lat, float* lse, void* stream);
+
 /* Static text for a status code. */
 const char* mla_status_string(int status);
 

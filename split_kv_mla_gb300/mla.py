@@ -27,6 +27,7 @@ MLA_WORKSPACE_HEADER_BYTES = 256
 MLA_DEVERR_BAD_SLOT = 1
 MLA_DEVERR_TIMEOUT = 2
 MLA_DEVERR_BAD_LENGTH = 4
+MLA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 HEADER = os.path.join(_build.ROOT, "include", "mla_decode.h")
 
 
@@ -84,6 +85,8 @@ def load(build_if_missing: bool = True):
             "mla_workspace_partials": (ctypes.c_int, [P, vp, ctypes.POINTER(vp),
                                                       ctypes.POINTER(vp)]),
             "mla_splitk_reduce": (ctypes.c_int, [vp, vp, i64, i32, i32, f32, vp, vp, vp]),
+            "mla_decode_noalloc": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, vp, i32, i32, i32,
+                                                  f32, f32, vp, vp, vp]),
             "mla_plan_force_splits": (ctypes.c_int, [P, i32]),
             "mla_workspace_reset": (ctypes.c_int, [vp, vp]),
             "mla_read_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), vp]),
@@ -285,3 +288,28 @@ def mla_read_device_error(workspace_t, stream=None) -> int:
     _check(load().mla_read_device_error(_dev_ptr(workspace_t, "workspace"), ctypes.byref(code),
                                         _stream_ptr(stream)), "mla_read_device_error")
     return int(code.value)
+
+
+def mla_decode_noalloc(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv_indptr,
+                       scale: float, kv_scale: float, o_lat, lse=None, stream=None):
+    """Dense decode through the entry point that allocates nothing: the library's
+    static scratch array stands in for the workspace.  For callers that cannot
+    allocate device memory; the caller passes preallocated outputs.  Calls that
+    overlap on the GPU share that scratch and race."""
+    for name, t in (("q_lat", q_lat), ("q_pe", q_pe), ("pool", pool), ("seq_lens", seq_lens),
+                    ("kv_indices", kv_indices), ("kv_indptr", kv_indptr), ("o_lat", o_lat)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    R, H = q_lat.shape[0], q_lat.shape[1]
+    batch = seq_lens.shape[0]
+    q_len = R // batch if batch else 1
+    pool_u8 = pool.view(torch.uint8) if pool.dtype != torch.uint8 else pool
+    rc = load().mla_decode_noalloc(
+        ctypes.byref(plan), _dev_ptr(q_lat, "q_lat", torch.bfloat16),
+        _dev_ptr(q_pe, "q_pe", torch.bfloat16), _dev_ptr(pool_u8, "pool"), pool_u8.shape[0],
+        _dev_ptr(seq_lens, "seq_lens", torch.int32), _dev_ptr(kv_indices, "kv_indices", torch.int32),
+        _dev_ptr(kv_indptr, "kv_indptr", torch.int32), batch, q_len, H, float(scale),
+        float(kv_scale), _dev_ptr(o_lat, "o_lat", torch.bfloat16), _dev_ptr(lse, "lse", torch.float32),
+        _stream_ptr(stream))
+    _check(rc, "mla_decode_noalloc")
+    return o_lat, lse

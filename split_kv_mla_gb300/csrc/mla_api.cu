@@ -14,16 +14,21 @@ constexpr int kSparseDv = 448, kSparseDr = 64;
 constexpr int kMaxHeads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Split-kernel geometry of the current variant.
-constexpr int kRowsPerCta = 16;
-constexpr int kBlockN = 32;
+// Split-kernel geometry: 128 keys per block; 16 query rows per CTA when a
+// request has at most 16 (heads x draft positions), else 32.
+constexpr int kBlockN = 128;
 
-// GB300 split rule constants (wave-fill, MLA-style branch of
-// hip_mha_decoding_num_partitions, re-derived for this kernel): the rule
-// targets `kWaves` resident waves of CTAs and at least kMinKeysPerSplit keys
-// per split; everything is a function of shapes and the SM count.
-constexpr int kWaves = 2;
-constexpr int kMinKeysPerSplit = 256;
+inline int32_t rows_per_cta_for(int64_t rows) { return rows <= 16 ? 16 : 32; }
+
+// GB300 split rule (the wave-fill idea of hip_mha_decoding_num_partitions,
+// re-derived for this kernel: one resident CTA per SM, 128-key blocks).  A
+// small cost model in microseconds picks the split count: waves of CTAs times
+// (blocks per CTA x block time + per-CTA fixed time), plus the reduce (a launch
+// and the fp32 partial traffic) when there is more than one split.
+constexpr double kBlockUs = 1.65;      // 128 x 576 B at one SM's share of HBM bandwidth
+constexpr double kCtaUs = 2.0;         // prologue, pipeline fill, epilogue
+constexpr double kReduceUs = 2.0;      // reduce launch and its latency chain
+constexpr double kBytesPerUs = 6.8e6;  // HBM bytes per microsecond
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -56,15 +61,49 @@ int64_t workspace_for(int64_t items, int ns, int d_v)
     return bytes;
 }
 
-// Split count for `ctas_per_split` CTAs per split and `keys` keys per request.
-int32_t gb300_splits(int64_t ctas_per_split, int64_t keys, int32_t sm_count)
+// Split count for `ctas_per_split` CTAs per split, `keys` keys per request and
+// `items` output rows (row x head) in the call.
+int32_t gb300_splits(int64_t ctas_per_split, int64_t keys, int64_t items, int32_t d_v,
+                     int32_t sm_count)
 {
-    int64_t target = (int64_t)kWaves * sm_count / (ctas_per_split > 0 ? ctas_per_split : 1);
-    int64_t by_keys = ceil_div(keys > 0 ? keys : 1, kMinKeysPerSplit);
-    int64_t ns = target < by_keys ? target : by_keys;
-    if (ns < 1) ns = 1;
-    if (ns > MLA_MAX_SPLITS) ns = MLA_MAX_SPLITS;
-    return (int32_t)ns;
+    const int64_t blocks = ceil_div(keys > 0 ? keys : 1, kBlockN);
+    const int64_t ctas = ctas_per_split > 0 ? ctas_per_split : 1;
+    const int64_t max_ns = blocks < MLA_MAX_SPLITS ? blocks : MLA_MAX_SPLITS;
+    double best = 0.0;
+    int32_t best_ns = 1;
+    for (int64_t ns = 1; ns <= max_ns; ++ns) {
+        const double waves = (double)ceil_div(ctas * ns, sm_count);
+        double t = waves * ((double)ceil_div(blocks, ns) * kBlockUs + kCtaUs);
+        if (ns > 1) t += kReduceUs + (double)items * ns * d_v * 4.0 * 2.0 / kBytesPerUs;
+        if (ns == 1 || t < best - 1e-9) {
+            best = t;
+            best_ns = (int32_t)ns;
+        }
+    }
+    return best_ns;
+}
+
+// Sparse split rule, following flashinfer.mla.cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits
+// ("Measured split rules") with this kernel's geometry: a chunk is 64
+// candidates and a CTA should keep at least one 128-key block (two chunks).
+// While the unsplit grid covers at most 40 % of the SMs, take the largest
+// power-of-two split keeping the grid within 80 % of the SMs and two chunks per
+// CTA; on a full grid, split 16-chunk work in two when the doubled grid ends in
+// a wave at least half full; otherwise run unsplit.
+int32_t sparse_splits(int64_t ctas, int64_t topk, int32_t sm_count)
+{
+    const int64_t chunks = ceil_div(topk > 0 ? topk : 1, 64);
+    if (chunks <= 2) return 1;
+    if (ctas * 10 <= (int64_t)sm_count * 4) {
+        int64_t ns = 1;
+        while (ctas * ns * 2 * 10 <= (int64_t)sm_count * 8 && chunks / (ns * 2) >= 2) ns *= 2;
+        return (int32_t)(ns < MLA_MAX_SPLITS ? ns : MLA_MAX_SPLITS);
+    }
+    if (ctas >= sm_count && chunks == 16) {
+        const int64_t tail = (2 * ctas) % sm_count;
+        if (tail == 0 || tail * 2 >= sm_count) return 2;
+    }
+    return 1;
 }
 
 void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32_t d_v,
@@ -73,13 +112,13 @@ void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32
     const int32_t rows = q_len * heads;
     std::memset(p, 0, sizeof *p);
     p->num_splits = ns;
-    p->rows_per_cta = kRowsPerCta;
+    p->rows_per_cta = rows_per_cta_for(rows);
     p->block_n = kBlockN;
-    p->head_blocks = (int32_t)ceil_div(rows, kRowsPerCta);
+    p->head_blocks = (int32_t)ceil_div(rows, p->rows_per_cta);
     p->grid_x = p->head_blocks;
     p->grid_y = ns;
     p->grid_z = batch;
-    p->variant = kVariantSimt;
+    p->variant = kVariantTc;
     p->workspace_bytes = workspace_for((int64_t)batch * rows, ns, d_v);
     p->batch = batch;
     p->q_len = q_len;
@@ -115,7 +154,8 @@ void carve(const mla_plan_t* plan, void* ws, int64_t items, SplitArgs* a)
 int run(const mla_plan_t* plan, SplitArgs& a, int64_t items, cudaStream_t stream,
         bool with_reduce)
 {
-    cudaError_t e = launch_split_simt(a, *plan, stream);
+    cudaError_t e = plan->variant == kVariantTc ? launch_split_tc(a, *plan, stream)
+                                                : launch_split_simt(a, *plan, stream);
     if (e != cudaSuccess) return MLA_ERR_LAUNCH_FAILED;
     if (with_reduce && plan->num_splits > 1) {
         e = launch_splitk_reduce(a.o_part, a.lse_part, items, plan->num_splits, plan->d_v,
@@ -170,9 +210,10 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
         return MLA_ERR_UNSUPPORTED_SHAPE;
     const int64_t rows = (int64_t)q_len * num_heads;
     if (rows > (1 << 20)) return MLA_ERR_UNSUPPORTED_SHAPE;
-    const int64_t head_blocks = ceil_div(rows, kRowsPerCta);
+    const int64_t head_blocks = ceil_div(rows, rows_per_cta_for(rows));
     const int64_t keys = batch > 0 ? ceil_div(total_keys, batch) : 0;
-    const int32_t ns = gb300_splits(head_blocks * (batch > 0 ? batch : 1), keys, sm_count);
+    const int32_t ns = gb300_splits(head_blocks * (batch > 0 ? batch : 1), keys,
+                                    (int64_t)batch * rows, d_v, sm_count);
     fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ns);
     return MLA_OK;
 }
@@ -187,8 +228,8 @@ int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk, 
         return MLA_ERR_UNSUPPORTED_SHAPE;
     const int32_t cap = max_splits == 0 ? MLA_MAX_SPLITS
                                         : (max_splits < MLA_MAX_SPLITS ? max_splits : MLA_MAX_SPLITS);
-    const int64_t head_blocks = ceil_div(num_heads, kRowsPerCta);
-    int32_t ns = gb300_splits(head_blocks * (num_tokens > 0 ? num_tokens : 1), topk, sm_count);
+    const int64_t head_blocks = ceil_div(num_heads, rows_per_cta_for(num_heads));
+    int32_t ns = sparse_splits(head_blocks * (num_tokens > 0 ? num_tokens : 1), topk, sm_count);
     if (ns > cap) ns = cap;
     fill_plan(out, num_tokens, 1, num_heads, d_v, d_rope, sm_count,
               (int64_t)num_tokens * topk, ns);
@@ -204,7 +245,8 @@ static int dense_call(const mla_plan_t* plan, const void* q_lat, const void* q_p
 {
     if (!plan) return MLA_ERR_INVALID_ARG;
     if (plan->batch != batch || plan->q_len != q_len || plan->num_heads != num_heads ||
-        plan->d_v != kDenseDv || plan->d_rope != kDenseDr || plan->variant != kVariantSimt ||
+        plan->d_v != kDenseDv || plan->d_rope != kDenseDr ||
+        (plan->variant != kVariantSimt && plan->variant != kVariantTc) ||
         plan->num_splits < 1 || plan->num_splits > MLA_MAX_SPLITS)
         return MLA_ERR_INVALID_ARG;
     if (batch == 0) return MLA_OK;
@@ -254,7 +296,8 @@ static int sparse_call(const mla_plan_t* plan, const void* q_nope, const void* q
 {
     if (!plan) return MLA_ERR_INVALID_ARG;
     if (plan->batch != num_tokens || plan->q_len != 1 || plan->num_heads != num_heads ||
-        plan->d_v != kSparseDv || plan->d_rope != kSparseDr || plan->variant != kVariantSimt ||
+        plan->d_v != kSparseDv || plan->d_rope != kSparseDr ||
+        (plan->variant != kVariantSimt && plan->variant != kVariantTc) ||
         plan->total_keys != (int64_t)num_tokens * topk || plan->num_splits < 1 ||
         plan->num_splits > MLA_MAX_SPLITS)
         return MLA_ERR_INVALID_ARG;

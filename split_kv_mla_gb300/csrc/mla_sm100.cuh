@@ -2,9 +2,9 @@
 // split kernel: mbarriers with bounded waits, TMA row gathers, tcgen05 tensor
 // memory, UMMA shared-memory and instruction descriptors.
 //
-// Every wait in here is bounded: after kSpinLimit polls (several seconds of
-// wall time with the suspend hint) it gives up and returns false, so a broken
-// pipeline ends the kernel with an error bit instead of hanging the GPU.
+// Every wait in here is bounded (a poll count or a wall-clock limit): it gives
+// up and returns false, so a broken pipeline ends the kernel with an error bit
+// instead of hanging the GPU.
 #pragma once
 #include <cstdint>
 
@@ -44,20 +44,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// One non-blocking poll of a phase.  (mbarrier.try_wait may suspend the thread
+// for a system-defined window, with or without a time hint, and measured on
+// GB300 a suspended waiter resumed about a microsecond after the phase had
+// completed; test_wait returns at once, so waits spin on it.)
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
 
-// Poll limit of a bounded wait; each poll may suspend up to the hint above.
+// Poll limit of a bounded wait.
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 // Wait for the phase with the given parity to complete; false on timeout.
@@ -68,28 +72,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
     return false;
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wall-clock bound of one pipeline wait inside the split kernel.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Cycle bound of one pipeline wait inside the split kernel (about a second).
+constexpr long long kWaitLimitCycles = 2000000000ll;
 
 // Wait for a phase, giving up (false) when *abort becomes nonzero or after
-// kWaitLimitNs; a timeout sets *abort so the CTA's other roles stop too.
+// kWaitLimitCycles SM cycles; a timeout sets *abort so the CTA's other roles
+// stop too.  With sleep_ns > 0 the waiter backs off with nanosleep after a few
+// polls, leaving issue slots to the warps that share its SM sub-partition.
+// (The SM cycle counter bounds the wait: reading the global timer costs about a
+// microsecond.)
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
-                                                   volatile int* abort)
+                                                   volatile int* abort, uint32_t sleep_ns = 0)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (sleep_ns != 0 && i > 4) __nanosleep(sleep_ns);
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (clock64() - t0 > kWaitLimitCycles) {
                 *abort = 1;
                 return false;
             }
@@ -120,6 +122,26 @@ __device__ __forceinline__ void tc_fence_before()
 __device__ __forceinline__ void tc_fence_after()
 {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---- cp.async ----------------------------------------------------------------------------------
+
+// 16-byte global -> shared copy through L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most n of this thread's committed groups are still pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
 }
 
 // ---- TMA ---------------------------------------------------------------------------------------

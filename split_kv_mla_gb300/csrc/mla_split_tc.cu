@@ -1,4 +1,4 @@
-// mla_split_tc.cu -- tcgen05 / TMA split kernel for absorbed-MLA decode (sm_103a).
+// mla_split_tc.cu -- tcgen05 split kernel for absorbed-MLA decode (sm_103a).
 //
 // One CTA computes one (request, head block, split) of the split-KV decode
 // (moonmath-ai/amd-kernels README, "MLA absorbed decode": one fused fp8 row per
@@ -21,18 +21,25 @@
 //   precise as rounding p to bf16).  hi and lo are stacked along N (2N MMA
 //   columns), so the big operand is read from shared memory once per MMA.
 //   kv_scale and the powers of two are folded into the logit and output scales.
-// * Warp roles.  Warp 0 gathers rows with TMA tile::gather4 (four slots per
-//   instruction, 128-byte latent boxes with 128B swizzle, a 64-byte RoPE box with
-//   64B swizzle) into a two-stage ring; warp 1 issues the tcgen05.mma
-//   (kind::f8f6f4, fp32 accumulators in TMEM) and commits to mbarriers; warps 2-5
-//   own one TMEM lane (= one key) each and run the online base-2 softmax.
+// * Warp roles.  Warps 0-3 gather the block's 128 rows with 16-byte cp.async
+//   (one fully coalesced warp instruction per 512-byte latent row, 128B-swizzled
+//   destinations; the 64-byte RoPE tails 64B-swizzled) into a two-stage ring;
+//   warp 4 issues the tcgen05.mma (kind::f8f6f4, fp32 accumulators in TMEM) and
+//   commits to mbarriers; warps 5-8 own one TMEM lane (= one key) each and run
+//   the online base-2 softmax.  Measured on GB300, random 576-byte rows gather at
+//   ~4.7 TB/s with four cp.async warps, ~2.2 TB/s with two, and ~2.2 TB/s with
+//   TMA tile::gather4 issued from one warp.
 // * Lazy rescaling.  A block only recomputes the running maxima when some logit
 //   exceeds them by more than kTau; otherwise p = 2^(s - m) stays below 2^kTau.
-//   O in TMEM is rescaled only at those (rare) blocks.
-// * Sums.  l (exact fp32 p, for the LSE) and lt (the fp8-split p actually fed to
-//   the MMA, for normalising O) are kept per thread and reduced once at the end.
-#include <cuda.h>
-#include <cudaTypedefs.h>
+//   The decision is one hardware barrier-reduction (bar.red.or) of the four
+//   softmax warps; O in TMEM is rescaled only at those (rare) blocks.
+// * Sums.  Each block's p (exact fp32, for the LSE) and p_hi + p_lo (what the
+//   MMA consumed, for normalising O) are summed over the warp's 32 keys with a
+//   transposing shuffle reduction, so each lane carries one row's running sums.
+// * Safety.  Every mbarrier wait is time-bounded and warp-uniform; the softmax
+//   warps meet at bar.sync only at points every one of them reaches, and agree
+//   on giving up through the same barrier-reduction, so a stuck pipeline ends
+//   with an error bit instead of a hang.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -47,9 +54,15 @@ namespace {
 using namespace sm100;
 
 constexpr int kBlockN = 128;          // keys per block (MMA M)
-constexpr int kThreads = 192;         // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kThreads = 288;         // warps 0-3 gather, warp 4 MMA, warps 5-8 softmax
+constexpr int kWarps = kThreads / 32;
+constexpr int kGatherWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kSoftmaxWarp0 = 5;
 constexpr float kTau = 2.f;           // lazy-rescale threshold, base-2 logit units
 constexpr float kShift = 6.f;         // p is fed as p * 2^kShift: at most 2^(kTau + kShift) = 256
+constexpr uint32_t kGatherSleepNs = 128;
+constexpr uint32_t kMmaSleepNs = 32;
 
 template <int N, bool SPARSE>
 struct Cfg {
@@ -69,21 +82,24 @@ struct Cfg {
     static constexpr uint32_t kTmemCols = (6 * NC <= 256) ? 256u : 512u;
     static constexpr uint32_t kColS = 0;                   // S^T buffers: [0, 2 NC)
     static constexpr uint32_t kColO = 2 * NC;              // O^T chunks:  [2 NC, 6 NC)
+    static constexpr int kGroups = kRowBytes / 8;          // 8-column query groups per row
+    static constexpr int kVec = (kGroups + 31) / 32;       // query groups per lane
+    static constexpr int kQRowsPerWarp = (N + kWarps - 1) / kWarps;
     static_assert(kOffQ % 1024 == 0 && kQChunkBytes % 1024 == 0, "128B-swizzle atoms");
     static_assert(kOffP % 16 == 0, "P tile alignment");
     static_assert(6 * NC <= 512, "TMEM columns");
+    static_assert(N * 512 * 4 <= 2 * kStageBytes, "epilogue staging fits in the stages");
 };
 
 struct Misc {
     uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], o_done;
-    uint64_t sm_bar;    // barrier of the 4 softmax warps (one arrival per warp)
     uint32_t tmem_base;
     int abort;
     int kvalid[2][kBlockN];
     float cq[32];       // per query row: raw dot -> base-2 logit
     int win[32];        // per query row: keys at positions < win are visible
     float red[4][32];   // cross-warp reduction scratch
-    int vote[2][4];
+    float fin[2][32];   // epilogue: 1 / lt and the base-2 LSE per row
 };
 
 template <int N, bool SPARSE>
@@ -108,9 +124,28 @@ __device__ __forceinline__ int tile_offset(int row, int c, int rows)
            (((kb >> 4) ^ ((row & 7) >> 1)) << 4) + (kb & 15);
 }
 
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t u)
+// x * 2^k, exact whenever the result is a normal fp32 number.
+__device__ __forceinline__ float mul_pow2(float x, int k)
 {
-    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+    if (k > 127) {
+        x *= __uint_as_float(254u << 23);
+        k -= 127;
+    } else if (k < -126) {
+        x *= __uint_as_float(1u << 23);
+        k += 126;
+    }
+    return x * __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+}
+
+// Power-of-two shift that brings max |q| into [128, 256).
+__device__ __forceinline__ int q_shift(float amax)
+{
+    if (!(amax > 0.f)) return 0;
+    const uint32_t bits = __float_as_uint(amax);
+    int e;  // amax = f * 2^e with f in [0.5, 1)
+    if ((bits >> 23) != 0) e = (int)(bits >> 23) - 126;
+    else frexpf(amax, &e);
+    return 8 - e;
 }
 
 // Split two fp32 values into e4m3 hi/lo bytes (pairs packed lo-byte first);
@@ -122,26 +157,6 @@ __device__ __forceinline__ float2 split_pair(float a, float b, uint16_t& hi, uin
     lo = f32x2_to_e4m3x2(a - h.x, b - h.y);
     const float2 l = e4m3x2_to_f32x2(lo);
     return make_float2(h.x + l.x, h.y + l.y);
-}
-
-// Bounded wait whose outcome is the same on every lane of the warp (all lanes
-// must call it), so no warp-collective instruction is reached divergently.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort)
-{
-    const bool ok = mbar_wait_or_abort(bar, parity, abort);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Barrier of the four softmax warps, built on an mbarrier so that it is
-// bounded: a warp that stopped early makes the others time out, not hang.
-// `phase` counts the barrier instances this thread has passed.
-__device__ __forceinline__ bool softmax_sync(uint64_t* bar, uint32_t& phase, volatile int* abort)
-{
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = warp_wait(bar, phase & 1, abort);
-    ++phase;
-    return ok;
 }
 
 // Reduce N values held by every lane of a warp (max or sum); afterwards lane l
@@ -173,37 +188,66 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane)
     return v[0];
 }
 
-// Reduce N per-thread values over the 128 softmax threads; every softmax
-// thread receives all N results in out[].  False if a barrier timed out.
-template <int N, bool MAX>
-__device__ __forceinline__ bool block_reduce(const float (&in)[N], float (&out)[N], Misc& ms,
-                                             int sw, int lane, uint32_t& phase,
-                                             volatile int* abort)
+// Barrier of the four softmax warps (id 1, 128 threads).  Only used at points
+// that all four warps always reach.
+__device__ __forceinline__ void softmax_bar()
 {
-    float v[N];
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// The same barrier, returning the OR of `v` over the four warps.
+__device__ __forceinline__ bool softmax_bar_or(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+// Bounded wait whose outcome is the same on every lane of the warp (all lanes
+// must call it), so no warp-collective instruction is reached divergently.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t sleep_ns = 0)
+{
+    const bool ok = mbar_wait_or_abort(bar, parity, abort, sleep_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// One TMEM row of N query-row columns: hi column n plus lo column N + n.
+template <int N>
+__device__ __forceinline__ void load_cols(uint32_t taddr, float (&s)[N])
+{
+    uint32_t r[32];
+    if (N == 16) {
+        tmem_ld32(taddr, r);
+        tmem_wait_ld();
 #pragma unroll
-    for (int n = 0; n < N; ++n) v[n] = in[n];
-    const float r = warp_transpose_reduce<N, MAX>(v, lane);
-    constexpr int kLanesPerValue = 32 / N;
-    if ((lane % kLanesPerValue) == 0) ms.red[sw][lane / kLanesPerValue] = r;
-    if (!softmax_sync(&ms.sm_bar, phase, abort)) return false;
+        for (int n = 0; n < N; ++n) s[n] = __uint_as_float(r[n]) + __uint_as_float(r[(n + N) & 31]);
+    } else {
+        tmem_ld32(taddr, r);
+        tmem_wait_ld();
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-        float x = ms.red[0][n];
+        for (int n = 0; n < N; ++n) s[n] = __uint_as_float(r[n & 31]);
+        tmem_ld32(taddr + 32, r);
+        tmem_wait_ld();
 #pragma unroll
-        for (int w = 1; w < 4; ++w) x = MAX ? fmaxf(x, ms.red[w][n]) : x + ms.red[w][n];
-        out[n] = x;
+        for (int n = 0; n < N; ++n) s[n] += __uint_as_float(r[n & 31]);
     }
-    return softmax_sync(&ms.sm_bar, phase, abort);
 }
 
 template <int N, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
-split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
-                const __grid_constant__ CUtensorMap tm_rope, const SplitArgs a)
+split_tc_kernel(const SplitArgs a)
 {
     using C = Cfg<N, SPARSE>;
     constexpr int NC = C::NC;
+    constexpr int kWidth = C::kRowBytes;
     extern __shared__ __align__(1024) uint8_t smem[];
     Misc& ms = *reinterpret_cast<Misc*>(smem + C::kOffMisc);
     volatile int* abort_flag = &ms.abort;
@@ -232,129 +276,182 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const int k1 = min(L, k0 + chunk);
     const int nblk = (k1 - k0 + kBlockN - 1) / kBlockN;
 
-    // ---- set-up: barriers, TMEM, the query tile --------------------------------------------
+    // ---- barriers and TMEM ----------------------------------------------------------------
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ms.kv_full[i], 1);
+            mbar_init(&ms.kv_full[i], kGatherWarps);   // one arrival per gather warp
             mbar_init(&ms.kv_empty[i], 1);
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.s_free[i], 4);
             mbar_init(&ms.p_full[i], 4);
         }
         mbar_init(&ms.o_done, 1);
-        mbar_init(&ms.sm_bar, 4);
         ms.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&ms.tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_lat);
-        if (C::kRope) tma_prefetch_desc(&tm_rope);
-    }
-    // Query rows: q scaled by 2^e so that max |q| is in [128, 256), then split
-    // into e4m3 hi (rows 0..N-1) and lo (rows N..2N-1).
-    constexpr int kWidth = C::kRowBytes;
-    constexpr int kPerLane = kWidth / 32;
-    uint8_t* qtile = smem + C::kOffQ;
-    for (int n = warp; n < N; n += kThreads / 32) {
-        const int idx = hb * N + n;
-        const bool valid = idx < rows_in_req;
-        int t = 0;
-        int64_t item = 0;
-        if (valid) {
-            t = idx / a.num_heads;
-            item = ((int64_t)b * a.q_len + t) * a.num_heads + idx % a.num_heads;
-        }
-        float qv[kPerLane];
-        float amax = 0.f;
-#pragma unroll
-        for (int k = 0; k < kPerLane; ++k) {
-            const int c = lane + 32 * k;
-            float v = 0.f;
-            if (valid)
-                v = c < a.d_v ? bf16_bits_to_f32(a.q_lat[item * a.d_v + c])
-                              : bf16_bits_to_f32(a.q_pe[item * a.d_rope + (c - a.d_v)]);
-            qv[k] = v;
-            amax = fmaxf(amax, fabsf(v));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        int e = 0;
-        if (amax > 0.f) frexpf(amax, &e);
-        const int sh = amax > 0.f ? 8 - e : 0;   // max |q * 2^sh| in [128, 256)
-#pragma unroll
-        for (int k = 0; k < kPerLane; k += 2) {
-            uint16_t hi, lo;
-            split_pair(ldexpf(qv[k], sh), ldexpf(qv[k + 1], sh), hi, lo);
-            const int c0 = lane + 32 * k, c1 = c0 + 32;
-            qtile[tile_offset(n, c0, NC)] = (uint8_t)(hi & 0xFF);
-            qtile[tile_offset(n, c1, NC)] = (uint8_t)(hi >> 8);
-            qtile[tile_offset(N + n, c0, NC)] = (uint8_t)(lo & 0xFF);
-            qtile[tile_offset(N + n, c1, NC)] = (uint8_t)(lo >> 8);
-        }
-        if (lane == 0) {
-            ms.cq[n] = valid ? a.logit_scale * ldexpf(1.f, -sh) : 0.f;
-            ms.win[n] = valid ? (L - a.q_len + t + 1) : -1;
-        }
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms.tmem_base;
     const uint32_t smem_base = smem_u32(smem);
 
-    if (warp == 0) {
-        // ================= TMA producer =================================================
-        const int32_t* list = a.kv_indices + base;
-        int32_t slot[4];
-        int ok[4];
-        auto load_slots = [&](int blk) {
-            const int kb = k0 + blk * kBlockN;
-            const int nk = min(kBlockN, k1 - kb);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = 4 * lane + q;
-                int32_t s = -1;
-                ok[q] = 0;
-                if (j < nk) {
-                    s = __ldg(list + kb + j);
-                    if (s >= 0 && (int64_t)s < a.pool_rows) ok[q] = 1;
-                    else if (!(SPARSE && s < 0)) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
-                }
-                slot[q] = ok[q] ? s : 0;   // masked keys load row 0: finite bytes, p = 0
-            }
-        };
-        if (nblk > 0) load_slots(0);
-        for (int blk = 0; blk < nblk; ++blk) {
-            const int st = blk & 1;
-            if (blk >= 2 && !warp_wait(&ms.kv_empty[st], ((blk - 2) >> 1) & 1, abort_flag))
-                break;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ms.kvalid[st][4 * lane + q] = ok[q];
-            // Every block gathers all 128 rows (masked keys read pool row 0), so the
-            // stage never holds stale or uninitialised bytes: a masked key's p is 0
-            // and 0 * (a finite fp8 value) is 0 in P.V.
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&ms.kv_full[st], (uint32_t)(kBlockN * kWidth));
-            __syncwarp();
-            {
-                uint8_t* stage = smem + C::kOffStage + st * C::kStageBytes;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tma_gather4(stage + c * C::kLatChunkBytes + lane * 512, &tm_lat, c * 128,
-                                slot[0], slot[1], slot[2], slot[3], &ms.kv_full[st]);
-                if (C::kRope)
-                    tma_gather4(stage + 4 * C::kLatChunkBytes + lane * 256, &tm_rope, 512,
-                                slot[0], slot[1], slot[2], slot[3], &ms.kv_full[st]);
-            }
-            if (blk + 1 < nblk) load_slots(blk + 1);
+    // ---- gather helpers (warps 0-3, 32 rows each) --------------------------------------------
+    const int32_t* list = a.kv_indices + base;
+    const int grow = warp * 32 + lane;   // a gather lane's row of every block
+    // Slot of this lane's row of block j; masked keys read pool row 0 (finite
+    // bytes; their p is 0).
+    auto load_slot = [&](int j, int& ok) -> int32_t {
+        const int kb = k0 + j * kBlockN;
+        const int nk = min(kBlockN, k1 - kb);
+        int32_t v = -1;
+        ok = 0;
+        if (grow < nk) {
+            v = __ldg(list + kb + grow);
+            if (v >= 0 && (int64_t)v < a.pool_rows) ok = 1;
+            else if (!(SPARSE && v < 0)) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
         }
-    } else if (warp == 1) {
+        return ok ? v : 0;
+    };
+    auto issue = [&](int j, int32_t sl, int ok) {
+        const int st = j & 1;
+        ms.kvalid[st][grow] = ok;
+        const uint32_t stage = smem_base + C::kOffStage + st * C::kStageBytes;
+        // latent / NoPE part: 512 bytes per row, lane copies bytes [16 lane, 16 lane + 16)
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+            const int r = warp * 32 + i;
+            const int32_t slot = __shfl_sync(0xffffffffu, sl, i);
+            const uint8_t* src = a.pool + (int64_t)slot * kWidth + lane * 16;
+            const uint32_t dst = stage + (lane >> 3) * C::kLatChunkBytes + (r >> 3) * 1024 +
+                                 (r & 7) * 128 + (((lane & 7) ^ (r & 7)) << 4);
+            cp_async16(dst, src);
+        }
+        if (C::kRope) {
+            // RoPE tails: 64 bytes per row, four lanes per row, eight rows per instruction
+#pragma unroll 1
+            for (int i8 = 0; i8 < 4; ++i8) {
+                const int ri = i8 * 8 + (lane >> 2);
+                const int r = warp * 32 + ri;
+                const int q = lane & 3;
+                const int32_t slot = __shfl_sync(0xffffffffu, sl, ri);
+                const uint8_t* src = a.pool + (int64_t)slot * kWidth + 512 + q * 16;
+                const uint32_t dst = stage + 4 * C::kLatChunkBytes + (r >> 3) * 512 +
+                                     (r & 7) * 64 + ((q ^ ((r & 7) >> 1)) << 4);
+                cp_async16(dst, src);
+            }
+        }
+        cp_async_commit();
+    };
+    int gok = 0;
+    int32_t gnext = 0;
+    if (warp < kGatherWarps && nblk > 0) {
+        // start the first two blocks before anything else
+        int ok;
+        int32_t sl = load_slot(0, ok);
+        issue(0, sl, ok);
+        if (nblk > 1) {
+            sl = load_slot(1, ok);
+            issue(1, sl, ok);
+        }
+        if (nblk > 2) gnext = load_slot(2, gok);
+    }
+
+    // ---- the query tile: one warp per row, every warp ------------------------------------------
+    // q is scaled by 2^sh so that max |q| is in [128, 256), then split into e4m3
+    // hi (tile rows 0..N-1) and lo (rows N..2N-1).
+    {
+        uint8_t* qtile = smem + C::kOffQ;
+        uint4 qv[C::kQRowsPerWarp][C::kVec];
+#pragma unroll
+        for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
+            const int n = warp + rr * kWarps;
+            const int idx = hb * N + n;
+            const bool valid = n < N && idx < rows_in_req;
+            int64_t item = 0;
+            if (valid)
+                item = ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads;
+#pragma unroll
+            for (int v = 0; v < C::kVec; ++v) {
+                const int c = (lane + 32 * v) * 8;
+                qv[rr][v] = make_uint4(0u, 0u, 0u, 0u);
+                if (valid && c < kWidth)
+                    qv[rr][v] = c < a.d_v
+                        ? __ldg(reinterpret_cast<const uint4*>(a.q_lat + item * a.d_v + c))
+                        : __ldg(reinterpret_cast<const uint4*>(a.q_pe + item * a.d_rope + (c - a.d_v)));
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
+            const int n = warp + rr * kWarps;
+            if (n >= N) break;
+            float amax = 0.f;
+#pragma unroll
+            for (int v = 0; v < C::kVec; ++v) {
+                const uint32_t w[4] = {qv[rr][v].x, qv[rr][v].y, qv[rr][v].z, qv[rr][v].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k] << 16)),
+                                             fabsf(__uint_as_float(w[k] & 0xFFFF0000u))));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const int sh = q_shift(amax);
+#pragma unroll
+            for (int v = 0; v < C::kVec; ++v) {
+                const int c = (lane + 32 * v) * 8;
+                if (c >= kWidth) continue;
+                const uint32_t w[4] = {qv[rr][v].x, qv[rr][v].y, qv[rr][v].z, qv[rr][v].w};
+                uint32_t hw[2], lw[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    uint16_t h0, l0, h1, l1;
+                    split_pair(mul_pow2(__uint_as_float(w[2 * k] << 16), sh),
+                               mul_pow2(__uint_as_float(w[2 * k] & 0xFFFF0000u), sh), h0, l0);
+                    split_pair(mul_pow2(__uint_as_float(w[2 * k + 1] << 16), sh),
+                               mul_pow2(__uint_as_float(w[2 * k + 1] & 0xFFFF0000u), sh), h1, l1);
+                    hw[k] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+                    lw[k] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+                }
+                *reinterpret_cast<uint2*>(qtile + tile_offset(n, c, NC)) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2*>(qtile + tile_offset(N + n, c, NC)) = make_uint2(lw[0], lw[1]);
+            }
+            if (lane == 0) {
+                const int idx = hb * N + n;
+                const bool valid = idx < rows_in_req;
+                ms.cq[n] = valid ? mul_pow2(a.logit_scale, -sh) : 0.f;
+                ms.win[n] = valid ? (L - a.q_len + idx / a.num_heads + 1) : -1;
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    if (warp < kGatherWarps) {
+        // ================= gather ============================================================
+        if (nblk > 0) {
+            for (int j = 0; j < nblk; ++j) {
+                if (j == 0 && nblk > 1) cp_async_wait<1>();
+                else cp_async_wait<0>();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms.kv_full[j & 1]);
+                if (j >= 1 && j + 1 < nblk) {
+                    // block j+1 reuses the stage of block j-1: wait for its P.V
+                    if (!warp_wait(&ms.kv_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag,
+                                   kGatherSleepNs))
+                        break;
+                    issue(j + 1, gnext, gok);
+                    if (j + 2 < nblk) gnext = load_slot(j + 2, gok);
+                }
+            }
+            cp_async_wait<0>();
+        }
+    } else if (warp == kMmaWarp) {
         // ================= MMA issuer =====================================================
         if (lane == 0 && nblk > 0) {
             const uint32_t id_qk = idesc_e4m3(128, NC, false, false);
@@ -378,9 +475,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             bool alive = true;
             for (int blk = 0; blk < nblk && alive; ++blk) {
                 const int st = blk & 1;
-                if (!mbar_wait_or_abort(&ms.kv_full[st], (blk >> 1) & 1, abort_flag)) break;
-                if (blk >= 2 &&
-                    !mbar_wait_or_abort(&ms.s_free[st], ((blk - 2) >> 1) & 1, abort_flag))
+                if (!mbar_wait_or_abort(&ms.kv_full[st], (blk >> 1) & 1, abort_flag, kMmaSleepNs))
+                    break;
+                if (blk >= 2 && !mbar_wait_or_abort(&ms.s_free[st], ((blk - 2) >> 1) & 1, abort_flag,
+                                                    kMmaSleepNs))
                     break;
                 tc_fence_after();
                 const uint32_t stage = smem_base + C::kOffStage + st * C::kStageBytes;
@@ -409,7 +507,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 umma_commit(&ms.s_full[st]);
                 if (blk >= 1) {
                     if (!mbar_wait_or_abort(&ms.p_full[(blk - 1) & 1], ((blk - 1) >> 1) & 1,
-                                            abort_flag)) {
+                                            abort_flag, kMmaSleepNs)) {
                         alive = false;
                         break;
                     }
@@ -419,7 +517,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
             if (alive && !*abort_flag) {
                 const int last = nblk - 1;
-                if (mbar_wait_or_abort(&ms.p_full[last & 1], (last >> 1) & 1, abort_flag)) {
+                if (mbar_wait_or_abort(&ms.p_full[last & 1], (last >> 1) & 1, abort_flag,
+                                       kMmaSleepNs)) {
                     tc_fence_after();
                     issue_pv(last);
                     umma_commit(&ms.o_done);
@@ -428,138 +527,116 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
         __syncwarp();
     } else {
-        // ================= softmax + epilogue (warps 2..5) =====================================
-        const int sw = warp - 2;                  // 0..3
+        // ================= softmax + epilogue (warps 5..8) =====================================
+        const int sw = warp - kSoftmaxWarp0;      // 0..3
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int ti = quad * 32 + lane;          // key within a block == TMEM lane
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-        float m_ref[N], l_part[N], lt_part[N], cq[N];
-        int win[N];
+        constexpr int kLanesPerRow = 32 / N;      // lanes holding the same row after a reduction
+        const int my_row = lane / kLanesPerRow;   // the row whose sums this lane carries
+        float m_ref[N];
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-            m_ref[n] = -CUDART_INF_F;
-            l_part[n] = 0.f;
-            lt_part[n] = 0.f;
-            cq[n] = ms.cq[n];
-            win[n] = ms.win[n];
-        }
+        for (int n = 0; n < N; ++n) m_ref[n] = -CUDART_INF_F;
+        float l_acc = 0.f, lt_acc = 0.f;          // running sums of row my_row over this warp's keys
         bool alive = true;
-        uint32_t sphase = 0;   // softmax barrier instances passed
         for (int blk = 0; blk < nblk; ++blk) {
             const int st = blk & 1;
             const uint32_t ph = (blk >> 1) & 1;
-            if (!warp_wait(&ms.kv_full[st], ph, abort_flag) ||
-                !warp_wait(&ms.s_full[st], ph, abort_flag)) {
-                alive = false;
-                break;
-            }
-            tc_fence_after();
-            const bool kval = ms.kvalid[st][ti] != 0;
-            const int j = k0 + blk * kBlockN + ti;
+            bool ok = warp_wait(&ms.kv_full[st], ph, abort_flag) &&
+                      warp_wait(&ms.s_full[st], ph, abort_flag);
             float s[N];
-            {
-                uint32_t r[32];
-                if (NC == 32) {
-                    tmem_ld32(tmem + lane_addr + C::kColS + st * NC, r);
-                    tmem_wait_ld();
+            if (ok) {
+                tc_fence_after();
+                load_cols<N>(tmem + lane_addr + C::kColS + st * NC, s);
+            } else {
 #pragma unroll
-                    for (int n = 0; n < N; ++n)
-                        s[n] = __uint_as_float(r[n]) + __uint_as_float(r[(n + N) & 31]);
-                } else {
-                    uint32_t r2[32];
-                    tmem_ld32(tmem + lane_addr + C::kColS + st * NC, r);
-                    tmem_ld32(tmem + lane_addr + C::kColS + st * NC + 32, r2);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int n = 0; n < N; ++n)
-                        s[n] = __uint_as_float(r[n & 31]) + __uint_as_float(r2[n & 31]);
-                }
+                for (int n = 0; n < N; ++n) s[n] = -CUDART_INF_F;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.s_free[st]);
+            const bool kval = ms.kvalid[st][ti] != 0;
+            const int j = k0 + blk * kBlockN + ti;
             bool need = false;
 #pragma unroll
             for (int n = 0; n < N; ++n) {
-                s[n] = (kval && j < win[n]) ? s[n] * cq[n] : -CUDART_INF_F;
+                s[n] = (kval && j < ms.win[n]) ? s[n] * ms.cq[n] : -CUDART_INF_F;
                 need |= s[n] > m_ref[n] + kTau;
             }
-            need = __any_sync(0xffffffffu, need);
-            if (lane == 0) ms.vote[blk & 1][sw] = need ? 1 : 0;
-            if (!softmax_sync(&ms.sm_bar, sphase, abort_flag)) {
+            if (softmax_bar_or(!ok || *abort_flag)) {
                 alive = false;
                 break;
             }
-            need = (ms.vote[blk & 1][0] | ms.vote[blk & 1][1] | ms.vote[blk & 1][2] |
-                    ms.vote[blk & 1][3]) != 0;
-            if (need) {
-                float bm[N];
-                if (!block_reduce<N, true>(s, bm, ms, sw, lane, sphase, abort_flag)) {
-                    alive = false;
-                    break;
-                }
+            if (softmax_bar_or(need)) {
+                // new running maxima: block max over the 128 keys, all four warps
+                float v[N];
+#pragma unroll
+                for (int n = 0; n < N; ++n) v[n] = s[n];
+                const float r = warp_transpose_reduce<N, true>(v, lane);
+                if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = r;
+                softmax_bar();
                 float alpha[N];
                 bool rescale = false;
 #pragma unroll
                 for (int n = 0; n < N; ++n) {
-                    const float mn = fmaxf(m_ref[n], bm[n]);
+                    const float bm = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]),
+                                           fmaxf(ms.red[2][n], ms.red[3][n]));
+                    const float mn = fmaxf(m_ref[n], bm);
                     float al = 1.f;
                     if (mn != -CUDART_INF_F)
                         al = (m_ref[n] == -CUDART_INF_F) ? 0.f : exp2f(m_ref[n] - mn);
                     alpha[n] = al;
                     rescale |= al != 1.f;
                     m_ref[n] = mn;
-                    l_part[n] *= al;
-                    lt_part[n] *= al;
                 }
+                float a_mine = 1.f;
+#pragma unroll
+                for (int n = 0; n < N; ++n)
+                    if (n == my_row) a_mine = alpha[n];
+                l_acc *= a_mine;
+                lt_acc *= a_mine;
                 if (rescale && blk > 0) {
                     // O^T holds blocks < blk: wait for the last P.V, then scale its columns.
-                    if (!warp_wait(&ms.kv_empty[(blk - 1) & 1], ((blk - 1) >> 1) & 1,
-                                   abort_flag)) {
-                        alive = false;
-                        break;
-                    }
-                    tc_fence_after();
+                    if (warp_wait(&ms.kv_empty[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag)) {
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                            for (int h = 0; h < NC / 32; ++h) {
+                                uint32_t rr[32];
+                                const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + h * 32;
+                                tmem_ld32(ta, rr);
+                                tmem_wait_ld();
 #pragma unroll
-                        for (int h = 0; h < NC / 32; ++h) {
-                            uint32_t r[32];
-                            const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + h * 32;
-                            tmem_ld32(ta, r);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha[(h * 32 + k) % N]);
-                            tmem_st32(ta, r);
+                                for (int k = 0; k < 32; ++k)
+                                    rr[k] = __float_as_uint(__uint_as_float(rr[k]) *
+                                                            alpha[(h * 32 + k) % N]);
+                                tmem_st32(ta, rr);
+                            }
                         }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
                 }
             }
             // P^T row ti: bytes [0, N) = p_hi, [N, 2N) = p_lo, of p * 2^kShift.
-            if (blk >= 2 && !warp_wait(&ms.kv_empty[st], ((blk - 2) >> 1) & 1, abort_flag)) {
-                alive = false;
-                break;
-            }
+            if (blk >= 2) warp_wait(&ms.kv_empty[st], ((blk - 2) >> 1) & 1, abort_flag);
+            float pt[N];
             uint32_t hiw[N / 4], low[N / 4];
 #pragma unroll
             for (int n = 0; n < N; n += 4) {
-                float p[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const float x = s[n + u];
-                    p[u] = (x == -CUDART_INF_F || m_ref[n + u] == -CUDART_INF_F)
-                               ? 0.f : exp2f(x - m_ref[n + u] + kShift);
-                    l_part[n + u] += p[u];
+                    s[n + u] = (x == -CUDART_INF_F || m_ref[n + u] == -CUDART_INF_F)
+                                   ? 0.f : exp2f(x - m_ref[n + u] + kShift);
                 }
                 uint16_t h0, l0, h1, l1;
-                const float2 v0 = split_pair(p[0], p[1], h0, l0);
-                const float2 v1 = split_pair(p[2], p[3], h1, l1);
-                lt_part[n] += v0.x;
-                lt_part[n + 1] += v0.y;
-                lt_part[n + 2] += v1.x;
-                lt_part[n + 3] += v1.y;
+                const float2 v0 = split_pair(s[n], s[n + 1], h0, l0);
+                const float2 v1 = split_pair(s[n + 2], s[n + 3], h1, l1);
+                pt[n] = v0.x;
+                pt[n + 1] = v0.y;
+                pt[n + 2] = v1.x;
+                pt[n + 3] = v1.y;
                 hiw[n / 4] = (uint32_t)h0 | ((uint32_t)h1 << 16);
                 low[n / 4] = (uint32_t)l0 | ((uint32_t)l1 << 16);
             }
@@ -575,58 +652,70 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.p_full[st]);
+            // running sums of this warp's 32 keys: lane ends up with row my_row
+            l_acc += warp_transpose_reduce<N, false>(s, lane);
+            lt_acc += warp_transpose_reduce<N, false>(pt, lane);
         }
 
         // ---- epilogue ------------------------------------------------------------------------
-        float l[N], lt[N];
-        alive = alive && !*abort_flag;
-        if (alive) alive = block_reduce<N, false>(l_part, l, ms, sw, lane, sphase, abort_flag);
-        if (alive) alive = block_reduce<N, false>(lt_part, lt, ms, sw, lane, sphase, abort_flag);
-        if (!alive) {
+        // row sums over all 128 keys, then 1/lt and the LSE per row
+        if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = l_acc;
+        softmax_bar();
+        float lsum = 0.f;
+        if (ti < N) lsum = ms.red[0][ti] + ms.red[1][ti] + ms.red[2][ti] + ms.red[3][ti];
+        softmax_bar();
+        if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = lt_acc;
+        softmax_bar();
+        if (ti < N) {
+            const float ltsum = ms.red[0][ti] + ms.red[1][ti] + ms.red[2][ti] + ms.red[3][ti];
+            float mr = 0.f;
 #pragma unroll
-            for (int n = 0; n < N; ++n) l[n] = lt[n] = 0.f;
+            for (int n = 0; n < N; ++n)
+                if (n == ti) mr = m_ref[n];
+            ms.fin[0][ti] = ltsum > 0.f ? 1.f / ltsum : 0.f;
+            ms.fin[1][ti] = lsum > 0.f ? mr + log2f(lsum) - kShift : -CUDART_INF_F;
         }
         const bool have_o = alive && nblk > 0 && warp_wait(&ms.o_done, 0, abort_flag);
         if (have_o) tc_fence_after();
-        const int ns = a.num_splits;
+        // O^T (+ hi/lo halves) -> ostage[n][d] fp32 in the now idle KV stages, then
+        // one compact cooperative loop writes normalized rows with 16-byte stores.
+        float* ostage = reinterpret_cast<float*>(smem + C::kOffStage);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-            const int d = c * 128 + ti;
             float o[N];
             if (have_o) {
-                uint32_t r[32];
-                if (NC == 32) {
-                    tmem_ld32(tmem + lane_addr + C::kColO + c * NC, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int n = 0; n < N; ++n)
-                        o[n] = __uint_as_float(r[n]) + __uint_as_float(r[(n + N) & 31]);
-                } else {
-                    uint32_t r2[32];
-                    tmem_ld32(tmem + lane_addr + C::kColO + c * NC, r);
-                    tmem_ld32(tmem + lane_addr + C::kColO + c * NC + 32, r2);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int n = 0; n < N; ++n)
-                        o[n] = __uint_as_float(r[n & 31]) + __uint_as_float(r2[n & 31]);
-                }
+                load_cols<N>(tmem + lane_addr + C::kColO + c * NC, o);
             } else {
 #pragma unroll
                 for (int n = 0; n < N; ++n) o[n] = 0.f;
             }
-            if (d >= C::kDv) continue;
 #pragma unroll
-            for (int n = 0; n < N; ++n) {
-                const int idx = hb * N + n;
-                if (idx >= rows_in_req) break;
-                const int64_t item =
-                    ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads;
-                const float val = lt[n] > 0.f ? o[n] / lt[n] : 0.f;
-                if (ns == 1)
-                    reinterpret_cast<__nv_bfloat16*>(a.o)[item * C::kDv + d] =
-                        __float2bfloat16_rn(val * a.out_scale);
-                else
-                    a.o_part[(item * ns + split) * C::kDv + d] = val;
+            for (int n = 0; n < N; ++n) ostage[n * 512 + c * 128 + ti] = o[n];
+        }
+        softmax_bar();
+        const int ns = a.num_splits;
+        constexpr int kQuads = C::kDv / 4;
+#pragma unroll 1
+        for (int it = ti; it < N * kQuads; it += 128) {
+            const int n = it / kQuads;
+            const int d = (it % kQuads) * 4;
+            const int idx = hb * N + n;
+            if (idx >= rows_in_req) continue;
+            const int64_t item =
+                ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads;
+            const float inv = ms.fin[0][n];
+            const float4 v = *reinterpret_cast<const float4*>(ostage + n * 512 + d);
+            if (ns == 1) {
+                const float f = inv * a.out_scale;
+                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * f, v.y * f);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * f, v.w * f);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(a.o + item * C::kDv + d) = pk;
+            } else {
+                *reinterpret_cast<float4*>(a.o_part + (item * ns + split) * C::kDv + d) =
+                    make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
             }
         }
         if (ti < N) {
@@ -634,14 +723,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             if (idx < rows_in_req) {
                 const int64_t item =
                     ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads;
-                float lsum = 0.f, mr = 0.f;
-#pragma unroll
-                for (int n = 0; n < N; ++n)
-                    if (n == ti) {
-                        lsum = l[n];
-                        mr = m_ref[n];
-                    }
-                const float lse2 = lsum > 0.f ? mr + log2f(lsum) - kShift : -CUDART_INF_F;
+                const float lse2 = ms.fin[1][ti];
                 if (ns == 1) {
                     if (a.lse) a.lse[item] = lse2;
                 } else {
@@ -649,15 +731,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 }
             }
         }
-        if (!alive || *abort_flag) {
-            if (lane == 0) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
-        }
+        if ((!alive || *abort_flag) && lane == 0) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
     }
 
     // ---- teardown -------------------------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
@@ -665,37 +745,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
 // ---- host side -------------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
-bool make_row_map(CUtensorMap* m, const void* pool, int64_t rows, int row_bytes, int box,
-                  CUtensorMapSwizzle sw)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-    cuuint64_t gstr[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t bdim[2] = {(cuuint32_t)box, 1};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), gdim, gstr, bdim, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int N, bool SPARSE>
-cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
-                           const mla_plan_t& plan, cudaStream_t stream)
+cudaError_t launch_variant(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream)
 {
     constexpr int smem = smem_bytes<N, SPARSE>();
     static std::once_flag once;
@@ -706,7 +757,7 @@ cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, cons
     });
     if (attr != cudaSuccess) return attr;
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-    split_tc_kernel<N, SPARSE><<<grid, kThreads, smem, stream>>>(lat, rope, a);
+    split_tc_kernel<N, SPARSE><<<grid, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -715,22 +766,12 @@ cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, cons
 cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream)
 {
     if (plan.grid_x <= 0 || plan.grid_y <= 0 || plan.grid_z <= 0) return cudaSuccess;
-    CUtensorMap lat, rope;
-    const int row_bytes = a.d_v + a.d_rope;
-    if (!make_row_map(&lat, a.pool, a.pool_rows, row_bytes, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    if (!a.sparse) {
-        if (!make_row_map(&rope, a.pool, a.pool_rows, row_bytes, 64, CU_TENSOR_MAP_SWIZZLE_64B))
-            return cudaErrorInvalidValue;
-    } else {
-        rope = lat;
-    }
     if (a.sparse) {
-        if (plan.rows_per_cta == 16) return launch_variant<16, true>(lat, rope, a, plan, stream);
-        return launch_variant<32, true>(lat, rope, a, plan, stream);
+        if (plan.rows_per_cta == 16) return launch_variant<16, true>(a, plan, stream);
+        return launch_variant<32, true>(a, plan, stream);
     }
-    if (plan.rows_per_cta == 16) return launch_variant<16, false>(lat, rope, a, plan, stream);
-    return launch_variant<32, false>(lat, rope, a, plan, stream);
+    if (plan.rows_per_cta == 16) return launch_variant<16, false>(a, plan, stream);
+    return launch_variant<32, false>(a, plan, stream);
 }
 
 }  // namespace mla

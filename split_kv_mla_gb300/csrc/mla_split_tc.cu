@@ -21,14 +21,15 @@
 //   precise as rounding p to bf16).  hi and lo are stacked along N (2N MMA
 //   columns), so the big operand is read from shared memory once per MMA.
 //   kv_scale and the powers of two are folded into the logit and output scales.
-// * Warp roles.  Warps 0-3 gather the block's 128 rows with 16-byte cp.async
-//   (one fully coalesced warp instruction per 512-byte latent row, 128B-swizzled
-//   destinations; the 64-byte RoPE tails 64B-swizzled) into a two-stage ring;
-//   warp 4 issues the tcgen05.mma (kind::f8f6f4, fp32 accumulators in TMEM) and
-//   commits to mbarriers; warps 5-8 own one TMEM lane (= one key) each and run
-//   the online base-2 softmax.  Measured on GB300, random 576-byte rows gather at
-//   ~4.7 TB/s with four cp.async warps, ~2.2 TB/s with two, and ~2.2 TB/s with
-//   TMA tile::gather4 issued from one warp.
+// * Warp roles.  Warps 0-3 gather the block's 128 rows with TMA tile::gather4
+//   (four slots per instruction; 128-byte latent boxes land 128B-swizzled, the
+//   64-byte RoPE box 64B-swizzled: exactly the K-major operand layout) into a
+//   two-stage ring, 32 rows per warp; warp 4 issues the tcgen05.mma
+//   (kind::f8f6f4, fp32 accumulators in TMEM) and commits to mbarriers; warps 5-8
+//   own one TMEM lane (= one key) each and run the online base-2 softmax.
+//   Measured on GB300, random 576-byte rows gather at ~4.8 TB/s when four warps
+//   issue gather4 (one issuing warp: ~2 TB/s); TMA keeps the bytes off the SM's
+//   load/store path, which the softmax warps' shared loads and shuffles use.
 // * Lazy rescaling.  A block only recomputes the running maxima when some logit
 //   exceeds them by more than kTau; otherwise p = 2^(s - m) stays below 2^kTau.
 //   The decision is one hardware barrier-reduction (bar.red.or) of the four
@@ -40,6 +41,8 @@
 //   warps meet at bar.sync only at points every one of them reaches, and agree
 //   on giving up through the same barrier-reduction, so a stuck pipeline ends
 //   with an error bit instead of a hang.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -243,7 +246,8 @@ __device__ __forceinline__ void load_cols(uint32_t taddr, float (&s)[N])
 
 template <int N, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
-split_tc_kernel(const SplitArgs a)
+split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
+                const __grid_constant__ CUtensorMap tm_rope, const SplitArgs a)
 {
     using C = Cfg<N, SPARSE>;
     constexpr int NC = C::NC;
@@ -299,7 +303,7 @@ split_tc_kernel(const SplitArgs a)
     const uint32_t tmem = ms.tmem_base;
     const uint32_t smem_base = smem_u32(smem);
 
-    // ---- gather helpers (warps 0-3, 32 rows each) --------------------------------------------
+    // ---- gather helpers (warps 0-3, 32 rows = 8 four-row groups each) ---------------------------
     const int32_t* list = a.kv_indices + base;
     const int grow = warp * 32 + lane;   // a gather lane's row of every block
     // Slot of this lane's row of block j; masked keys read pool row 0 (finite
@@ -316,40 +320,48 @@ split_tc_kernel(const SplitArgs a)
         }
         return ok ? v : 0;
     };
+    // Block j into stage j & 1: the warp's 8 groups x (4 latent boxes + RoPE box),
+    // spread over its lanes; every block loads all 128 rows.
+    constexpr int kBoxes = C::kRope ? 5 : 4;
     auto issue = [&](int j, int32_t sl, int ok) {
         const int st = j & 1;
         ms.kvalid[st][grow] = ok;
-        const uint32_t stage = smem_base + C::kOffStage + st * C::kStageBytes;
-        // latent / NoPE part: 512 bytes per row, lane copies bytes [16 lane, 16 lane + 16)
-#pragma unroll 4
-        for (int i = 0; i < 32; ++i) {
-            const int r = warp * 32 + i;
-            const int32_t slot = __shfl_sync(0xffffffffu, sl, i);
-            const uint8_t* src = a.pool + (int64_t)slot * kWidth + lane * 16;
-            const uint32_t dst = stage + (lane >> 3) * C::kLatChunkBytes + (r >> 3) * 1024 +
-                                 (r & 7) * 128 + (((lane & 7) ^ (r & 7)) << 4);
-            cp_async16(dst, src);
-        }
-        if (C::kRope) {
-            // RoPE tails: 64 bytes per row, four lanes per row, eight rows per instruction
-#pragma unroll 1
-            for (int i8 = 0; i8 < 4; ++i8) {
-                const int ri = i8 * 8 + (lane >> 2);
-                const int r = warp * 32 + ri;
-                const int q = lane & 3;
-                const int32_t slot = __shfl_sync(0xffffffffu, sl, ri);
-                const uint8_t* src = a.pool + (int64_t)slot * kWidth + 512 + q * 16;
-                const uint32_t dst = stage + 4 * C::kLatChunkBytes + (r >> 3) * 512 +
-                                     (r & 7) * 64 + ((q ^ ((r & 7) >> 1)) << 4);
-                cp_async16(dst, src);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&ms.kv_full[st], 32u * kWidth);
+        __syncwarp();
+        uint8_t* stage = smem + C::kOffStage + st * C::kStageBytes;
+        // item = (group, box); lane handles items lane and lane + 32.  Every
+        // shuffle runs on all 32 lanes (source lanes clamped for idle items);
+        // only the copies themselves are predicated.
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int item = lane + 32 * pass;
+            const bool active = item < 8 * kBoxes;
+            const int gl = active ? item / kBoxes : 0;
+            const int c = active ? item % kBoxes : 0;
+            const int32_t r0 = __shfl_sync(0xffffffffu, sl, 4 * gl);
+            const int32_t r1 = __shfl_sync(0xffffffffu, sl, 4 * gl + 1);
+            const int32_t r2 = __shfl_sync(0xffffffffu, sl, 4 * gl + 2);
+            const int32_t r3 = __shfl_sync(0xffffffffu, sl, 4 * gl + 3);
+            if (active) {
+                const int g = warp * 8 + gl;
+                if (c < 4)
+                    tma_gather4(stage + c * C::kLatChunkBytes + g * 512, &tm_lat, c * 128,
+                                r0, r1, r2, r3, &ms.kv_full[st]);
+                else
+                    tma_gather4(stage + 4 * C::kLatChunkBytes + g * 256, &tm_rope, 512,
+                                r0, r1, r2, r3, &ms.kv_full[st]);
             }
         }
-        cp_async_commit();
     };
     int gok = 0;
     int32_t gnext = 0;
     if (warp < kGatherWarps && nblk > 0) {
         // start the first two blocks before anything else
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_lat);
+            if (C::kRope) tma_prefetch_desc(&tm_rope);
+        }
         int ok;
         int32_t sl = load_slot(0, ok);
         issue(0, sl, ok);
@@ -433,24 +445,21 @@ split_tc_kernel(const SplitArgs a)
 
     if (warp < kGatherWarps) {
         // ================= gather ============================================================
-        if (nblk > 0) {
-            for (int j = 0; j < nblk; ++j) {
-                if (j == 0 && nblk > 1) cp_async_wait<1>();
-                else cp_async_wait<0>();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ms.kv_full[j & 1]);
-                if (j >= 1 && j + 1 < nblk) {
-                    // block j+1 reuses the stage of block j-1: wait for its P.V
-                    if (!warp_wait(&ms.kv_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag,
-                                   kGatherSleepNs))
-                        break;
-                    issue(j + 1, gnext, gok);
-                    if (j + 2 < nblk) gnext = load_slot(j + 2, gok);
-                }
-            }
-            cp_async_wait<0>();
+        // block j reuses the stage of block j-2: wait for its P.V, then load
+        int issued = nblk < 2 ? nblk : 2;
+        for (int j = 2; j < nblk; ++j) {
+            if (!warp_wait(&ms.kv_empty[j & 1], ((j - 2) >> 1) & 1, abort_flag, kGatherSleepNs))
+                break;
+            issue(j, gnext, gok);
+            issued = j + 1;
+            if (j + 1 < nblk) gnext = load_slot(j + 1, gok);
         }
+        // Never leave the CTA with loads in flight: the last two issued blocks
+        // (earlier ones were consumed before their stage was reused) must land.
+        // A fresh wait flag keeps this drain going even after an abort.
+        volatile int drain_abort = 0;
+        for (int j = issued - 2; j < issued; ++j)
+            if (j >= 0) warp_wait(&ms.kv_full[j & 1], (j >> 1) & 1, &drain_abort, kGatherSleepNs);
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer =====================================================
         if (lane == 0 && nblk > 0) {
@@ -745,8 +754,39 @@ split_tc_kernel(const SplitArgs a)
 
 // ---- host side -------------------------------------------------------------------------------
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// 2-D uint8 map of the pool (row_bytes columns x rows) with one-row boxes of
+// `box` columns: the shape tile::gather4 reads.
+bool make_row_map(CUtensorMap* m, const void* pool, int64_t rows, int row_bytes, int box,
+                  CUtensorMapSwizzle sw)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t gstr[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t bdim[2] = {(cuuint32_t)box, 1};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), gdim, gstr, bdim, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int N, bool SPARSE>
-cudaError_t launch_variant(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream)
+cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
+                           const mla_plan_t& plan, cudaStream_t stream)
 {
     constexpr int smem = smem_bytes<N, SPARSE>();
     static std::once_flag once;
@@ -757,7 +797,7 @@ cudaError_t launch_variant(const SplitArgs& a, const mla_plan_t& plan, cudaStrea
     });
     if (attr != cudaSuccess) return attr;
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-    split_tc_kernel<N, SPARSE><<<grid, kThreads, smem, stream>>>(a);
+    split_tc_kernel<N, SPARSE><<<grid, kThreads, smem, stream>>>(lat, rope, a);
     return cudaGetLastError();
 }
 
@@ -766,12 +806,22 @@ cudaError_t launch_variant(const SplitArgs& a, const mla_plan_t& plan, cudaStrea
 cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream)
 {
     if (plan.grid_x <= 0 || plan.grid_y <= 0 || plan.grid_z <= 0) return cudaSuccess;
-    if (a.sparse) {
-        if (plan.rows_per_cta == 16) return launch_variant<16, true>(a, plan, stream);
-        return launch_variant<32, true>(a, plan, stream);
+    CUtensorMap lat, rope;
+    const int row_bytes = a.d_v + a.d_rope;
+    if (!make_row_map(&lat, a.pool, a.pool_rows, row_bytes, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!a.sparse) {
+        if (!make_row_map(&rope, a.pool, a.pool_rows, row_bytes, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    } else {
+        rope = lat;
     }
-    if (plan.rows_per_cta == 16) return launch_variant<16, false>(a, plan, stream);
-    return launch_variant<32, false>(a, plan, stream);
+    if (a.sparse) {
+        if (plan.rows_per_cta == 16) return launch_variant<16, true>(lat, rope, a, plan, stream);
+        return launch_variant<32, true>(lat, rope, a, plan, stream);
+    }
+    if (plan.rows_per_cta == 16) return launch_variant<16, false>(lat, rope, a, plan, stream);
+    return launch_variant<32, false>(lat, rope, a, plan, stream);
 }
 
 }  // namespace mla

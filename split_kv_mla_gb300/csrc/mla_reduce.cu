@@ -64,7 +64,26 @@ splitk_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__
     if (c < d_v) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         const float* op = o_part + row * (int64_t)num_splits * d_v + c;
-        for (int s = 0; s < num_splits; ++s) {
+        // Loads of kUnroll splits are issued before their sums, so the memory
+        // latency is paid once per group, not once per split; the sums still run
+        // in increasing split order.
+        constexpr int kUnroll = 8;
+        int s = 0;
+        for (; s + kUnroll <= num_splits; s += kUnroll) {
+            float4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                v[u] = __ldg(reinterpret_cast<const float4*>(op + (int64_t)(s + u) * d_v));
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const float w = w_s[s + u];
+                acc.x += w * v[u].x;
+                acc.y += w * v[u].y;
+                acc.z += w * v[u].z;
+                acc.w += w * v[u].w;
+            }
+        }
+        for (; s < num_splits; ++s) {
             const float w = w_s[s];
             const float4 v = __ldg(reinterpret_cast<const float4*>(op + (int64_t)s * d_v));
             acc.x += w * v.x;

@@ -99,7 +99,7 @@ struct Misc {
     uint32_t tmem_base;
     int abort;
     int kvalid[2][kBlockN];
-    float cq[32];       // per query row: raw dot -> base-2 logit
+    alignas(16) float cq[32];   // per query row: raw dot -> base-2 logit
     int win[32];        // per query row: keys at positions < win are visible
     float red[4][32];   // cross-warp reduction scratch
     float fin[2][32];   // epilogue: 1 / lt and the base-2 LSE per row
@@ -566,11 +566,34 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             if (lane == 0) mbar_arrive(&ms.s_free[st]);
             const bool kval = ms.kvalid[st][ti] != 0;
             const int j = k0 + blk * kBlockN + ti;
-            bool need = false;
+            // Per-row logit scales as 16-byte loads issued together, and a
+            // branch-free mask.  The draft window only bites in blocks that reach
+            // the last q_len - 1 positions of the request (kval already drops keys
+            // beyond the split); elsewhere every row sees every valid key.
+            const bool tail = k0 + (blk + 1) * kBlockN > L - a.q_len + 1;
+            float cq[N];
 #pragma unroll
-            for (int n = 0; n < N; ++n) {
-                s[n] = (kval && j < ms.win[n]) ? s[n] * ms.cq[n] : -CUDART_INF_F;
-                need |= s[n] > m_ref[n] + kTau;
+            for (int g = 0; g < N / 4; ++g) {
+                const float4 v = reinterpret_cast<const float4*>(ms.cq)[g];
+                cq[4 * g] = v.x;
+                cq[4 * g + 1] = v.y;
+                cq[4 * g + 2] = v.z;
+                cq[4 * g + 3] = v.w;
+            }
+            bool need = false;
+            if (!tail) {
+#pragma unroll
+                for (int n = 0; n < N; ++n) {
+                    s[n] = kval ? s[n] * cq[n] : -CUDART_INF_F;
+                    need |= s[n] > m_ref[n] + kTau;
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < N; ++n) {
+                    const bool vis = kval && j < ms.win[n];
+                    s[n] = vis ? s[n] * cq[n] : -CUDART_INF_F;
+                    need |= s[n] > m_ref[n] + kTau;
+                }
             }
             if (softmax_bar_or(!ok || *abort_flag)) {
                 alive = false;

@@ -64,6 +64,8 @@ constexpr int kMmaWarp = 4;
 constexpr int kSoftmaxWarp0 = 5;
 constexpr float kTau = 2.f;           // lazy-rescale threshold, base-2 logit units
 constexpr float kShift = 6.f;         // p is fed as p * 2^kShift: at most 2^(kTau + kShift) = 256
+constexpr int kQWarps = kWarps - kMmaWarp;   // warps 4-8 split the query tile
+constexpr uint32_t kQBar = 2;                // their named barrier (id 1 is the softmax one)
 constexpr uint32_t kGatherSleepNs = 128;
 constexpr uint32_t kMmaSleepNs = 32;
 
@@ -87,7 +89,7 @@ struct Cfg {
     static constexpr uint32_t kColO = 2 * NC;              // O^T chunks:  [2 NC, 6 NC)
     static constexpr int kGroups = kRowBytes / 8;          // 8-column query groups per row
     static constexpr int kVec = (kGroups + 31) / 32;       // query groups per lane
-    static constexpr int kQRowsPerWarp = (N + kWarps - 1) / kWarps;
+    static constexpr int kQRowsPerWarp = (N + kQWarps - 1) / kQWarps;
     static_assert(kOffQ % 1024 == 0 && kQChunkBytes % 1024 == 0, "128B-swizzle atoms");
     static_assert(kOffP % 16 == 0, "P tile alignment");
     static_assert(6 * NC <= 512, "TMEM columns");
@@ -308,18 +310,22 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const int grow = warp * 32 + lane;   // a gather lane's row of every block
     // Slot of this lane's row of block j; masked keys read pool row 0 (finite
     // bytes; their p is 0).
-    auto load_slot = [&](int j, int& ok) -> int32_t {
+    auto raw_slot = [&](int j) -> int32_t {   // the index itself (-1 past the split)
         const int kb = k0 + j * kBlockN;
         const int nk = min(kBlockN, k1 - kb);
-        int32_t v = -1;
+        return grow < nk ? __ldg(list + kb + grow) : -1;
+    };
+    auto check_slot = [&](int j, int32_t v, int& ok) -> int32_t {
+        const int kb = k0 + j * kBlockN;
+        const int nk = min(kBlockN, k1 - kb);
         ok = 0;
         if (grow < nk) {
-            v = __ldg(list + kb + grow);
             if (v >= 0 && (int64_t)v < a.pool_rows) ok = 1;
             else if (!(SPARSE && v < 0)) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
         }
         return ok ? v : 0;
     };
+    auto load_slot = [&](int j, int& ok) -> int32_t { return check_slot(j, raw_slot(j), ok); };
     // Block j into stage j & 1: the warp's 8 groups x (4 latent boxes + RoPE box),
     // spread over its lanes; every block loads all 128 rows.
     constexpr int kBoxes = C::kRope ? 5 : 4;
@@ -362,25 +368,31 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             tma_prefetch_desc(&tm_lat);
             if (C::kRope) tma_prefetch_desc(&tm_rope);
         }
+        // the three index loads are in flight together
+        const int32_t v0 = raw_slot(0);
+        const int32_t v1 = nblk > 1 ? raw_slot(1) : -1;
+        const int32_t v2 = nblk > 2 ? raw_slot(2) : -1;
         int ok;
-        int32_t sl = load_slot(0, ok);
+        int32_t sl = check_slot(0, v0, ok);
         issue(0, sl, ok);
         if (nblk > 1) {
-            sl = load_slot(1, ok);
+            sl = check_slot(1, v1, ok);
             issue(1, sl, ok);
         }
-        if (nblk > 2) gnext = load_slot(2, gok);
+        if (nblk > 2) gnext = check_slot(2, v2, gok);
     }
 
-    // ---- the query tile: one warp per row, every warp ------------------------------------------
+    // ---- the query tile: one warp per row, warps 4-8 ---------------------------------------------
     // q is scaled by 2^sh so that max |q| is in [128, 256), then split into e4m3
-    // hi (tile rows 0..N-1) and lo (rows N..2N-1).
-    {
+    // hi (tile rows 0..N-1) and lo (rows N..2N-1).  The gather warps go on
+    // loading meanwhile; the MMA warp waits for the tile at the warps' barrier.
+    if (warp >= kMmaWarp) {
+        const int qw = warp - kMmaWarp;
         uint8_t* qtile = smem + C::kOffQ;
         uint4 qv[C::kQRowsPerWarp][C::kVec];
 #pragma unroll
         for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
-            const int n = warp + rr * kWarps;
+            const int n = qw + rr * kQWarps;
             const int idx = hb * N + n;
             const bool valid = n < N && idx < rows_in_req;
             int64_t item = 0;
@@ -398,7 +410,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
 #pragma unroll
         for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
-            const int n = warp + rr * kWarps;
+            const int n = qw + rr * kQWarps;
             if (n >= N) break;
             float amax = 0.f;
 #pragma unroll
@@ -440,8 +452,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
         }
     }
-    fence_proxy_async_smem();
-    __syncthreads();
+    if (warp >= kMmaWarp) {
+        fence_proxy_async_smem();
+        asm volatile("bar.sync %0, %1;" ::"n"(kQBar), "n"(kQWarps * 32) : "memory");
+    }
 
     if (warp < kGatherWarps) {
         // ================= gather ============================================================
@@ -462,58 +476,58 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             if (j >= 0) warp_wait(&ms.kv_full[j & 1], (j >> 1) & 1, &drain_abort, kGatherSleepNs);
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer =====================================================
+        // Order per block j: P.V of block j-1 as soon as its P is ready (frees that
+        // stage for the gather of block j+1 as early as possible), then Q.K^T of
+        // block j.  Descriptors are built once per stage and advanced by adding
+        // the byte offset / 16 to their address field (shared memory < 256 KB, so
+        // the 14-bit field never carries).
         if (lane == 0 && nblk > 0) {
             const uint32_t id_qk = idesc_e4m3(128, NC, false, false);
             const uint32_t id_pv = idesc_e4m3(128, NC, true, true);
+            const uint32_t stage0 = smem_base + C::kOffStage;
+            const uint32_t qb = smem_base + C::kOffQ;
+            const uint64_t qk_a_lat = smem_desc(stage0, 16, 1024, kSw128);
+            const uint64_t qk_a_rope = smem_desc(stage0 + 4 * C::kLatChunkBytes, 16, 512, kSw64);
+            const uint64_t qk_b_lat = smem_desc(qb, 16, 1024, kSw128);
+            const uint64_t qk_b_rope = smem_desc(qb + 4 * C::kQChunkBytes, 16, 512, kSw64);
+            const uint64_t pv_a = smem_desc(stage0, C::kLatChunkBytes, 1024, kSw128);
+            const uint64_t pv_b = smem_desc(smem_base + C::kOffP, 128, 2048, kSwNone);
             auto issue_pv = [&](int blk) {
                 const int st = blk & 1;
-                const uint32_t stage = smem_base + C::kOffStage + st * C::kStageBytes;
-                const uint32_t pt = smem_base + C::kOffP + st * C::kPBytes;
+                const uint64_t a0 = pv_a + (uint64_t)((st * C::kStageBytes) >> 4);
+                const uint64_t b0 = pv_b + (uint64_t)((st * C::kPBytes) >> 4);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc(stage + c * C::kLatChunkBytes + kk * 4096,
-                                                      C::kLatChunkBytes, 1024, kSw128);
-                        const uint64_t bd = smem_desc(pt + kk * 512, 128, 2048, kSwNone);
-                        umma_f8(tmem + C::kColO + c * NC, ad, bd, id_pv,
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_f8(tmem + C::kColO + c * NC,
+                                a0 + (uint64_t)((c * C::kLatChunkBytes + kk * 4096) >> 4),
+                                b0 + (uint64_t)((kk * 512) >> 4), id_pv,
                                 (blk > 0 || kk > 0) ? 1u : 0u);
-                    }
                 umma_commit(&ms.kv_empty[st]);
             };
-            bool alive = true;
-            for (int blk = 0; blk < nblk && alive; ++blk) {
+            auto issue_qk = [&](int blk) {
                 const int st = blk & 1;
-                if (!mbar_wait_or_abort(&ms.kv_full[st], (blk >> 1) & 1, abort_flag, kMmaSleepNs))
-                    break;
-                if (blk >= 2 && !mbar_wait_or_abort(&ms.s_free[st], ((blk - 2) >> 1) & 1, abort_flag,
-                                                    kMmaSleepNs))
-                    break;
-                tc_fence_after();
-                const uint32_t stage = smem_base + C::kOffStage + st * C::kStageBytes;
-                const uint32_t qb = smem_base + C::kOffQ;
+                const uint64_t soff = (uint64_t)((st * C::kStageBytes) >> 4);
                 const uint32_t d = tmem + C::kColS + st * NC;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad =
-                            smem_desc(stage + c * C::kLatChunkBytes + kk * 32, 16, 1024, kSw128);
-                        const uint64_t bd =
-                            smem_desc(qb + c * C::kQChunkBytes + kk * 32, 16, 1024, kSw128);
-                        umma_f8(d, ad, bd, id_qk, (c > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_f8(d, qk_a_lat + soff + (uint64_t)((c * C::kLatChunkBytes + kk * 32) >> 4),
+                                qk_b_lat + (uint64_t)((c * C::kQChunkBytes + kk * 32) >> 4), id_qk,
+                                (c > 0 || kk > 0) ? 1u : 0u);
                 if (C::kRope) {
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint64_t ad =
-                            smem_desc(stage + 4 * C::kLatChunkBytes + kk * 32, 16, 512, kSw64);
-                        const uint64_t bd =
-                            smem_desc(qb + 4 * C::kQChunkBytes + kk * 32, 16, 512, kSw64);
-                        umma_f8(d, ad, bd, id_qk, 1u);
-                    }
+                    for (int kk = 0; kk < 2; ++kk)
+                        umma_f8(d, qk_a_rope + soff + (uint64_t)((kk * 32) >> 4),
+                                qk_b_rope + (uint64_t)((kk * 32) >> 4), id_qk, 1u);
                 }
                 umma_commit(&ms.s_full[st]);
+            };
+            bool alive = true;
+            for (int blk = 0; blk < nblk && alive; ++blk) {
+                const int st = blk & 1;
                 if (blk >= 1) {
                     if (!mbar_wait_or_abort(&ms.p_full[(blk - 1) & 1], ((blk - 1) >> 1) & 1,
                                             abort_flag, kMmaSleepNs)) {
@@ -523,6 +537,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                     tc_fence_after();
                     issue_pv(blk - 1);
                 }
+                if (!mbar_wait_or_abort(&ms.kv_full[st], (blk >> 1) & 1, abort_flag, kMmaSleepNs) ||
+                    (blk >= 2 && !mbar_wait_or_abort(&ms.s_free[st], ((blk - 2) >> 1) & 1,
+                                                     abort_flag, kMmaSleepNs))) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_qk(blk);
             }
             if (alive && !*abort_flag) {
                 const int last = nblk - 1;

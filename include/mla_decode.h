@@ -90,7 +90,9 @@ typedef struct {
     int32_t block_n;         /* keys per pipeline block */
     int32_t head_blocks;     /* CTAs sharing one (request, split) */
     int32_t grid_x, grid_y, grid_z;  /* head_blocks, num_splits, batch (or tokens) */
-    int32_t variant;         /* kernel variant chosen for the shape */
+    int32_t variant;         /* kernel variant: 2 = tcgen05 split kernel, then the
+                                split-K reduce kernel when num_splits > 1;
+                                other values are rejected (MLA_ERR_INVALID_ARG) */
     int64_t workspace_bytes; /* bytes of device workspace the call needs */
     int32_t batch, q_len, num_heads, d_v, d_rope, sm_count;
     int64_t total_keys;      /* dense: kv_indices length; sparse: tokens * topk */
@@ -110,9 +112,10 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
  * Sparse top-k plan (flashinfer.mla.cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits:
  * one decode call's (num_splits, chunks per CTA) from tokens, heads, top-k and
  * the SM count; "[Perf] pa_decode_sparse ..." issue: 64 heads, 448 NoPE + 64
- * RoPE columns, top-k 2048).  d_v must be 448 and d_rope 64.  max_splits bounds
- * num_splits (0 = MLA_MAX_SPLITS); a bound below what the top-k needs is
- * rejected with MLA_ERR_UNSUPPORTED_SHAPE (plan_splits raises likewise).
+ * RoPE columns, top-k 2048).  d_v must be 448 and d_rope 64.  max_splits caps
+ * num_splits (0 = MLA_MAX_SPLITS).  Every split count from 1 up is valid for
+ * this kernel (a split may even be empty), so a small cap costs speed only and
+ * is never an error.
  */
 int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
                            int32_t d_v, int32_t d_rope, int32_t sm_count, int32_t max_splits,
@@ -120,7 +123,9 @@ int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
 
 /*
  * Dense decode: enqueues the split kernel and, when plan->num_splits > 1, the
- * split-K reduce.  Layouts (row-major, contiguous):
+ * split-K reduce (launched as a programmatic dependent of the split kernel, so
+ * it is scheduled while the split kernel drains).  Layouts (row-major,
+ * contiguous):
  *   q_lat    bf16 [batch*q_len, num_heads, 512]   row r = b*q_len + t
  *   q_pe     bf16 [batch*q_len, num_heads, 64]
  *   pool     e4m3fn bytes [pool_rows, 576] (a [pool_rows, 1, 576] tensor), 16-byte aligned
@@ -195,7 +200,9 @@ int mla_workspace_partials(const mla_plan_t* plan, void* workspace, float** o_pa
  *   M = max_s lse_part[row, s];  w_s = 2^(lse_part[row, s] - M)
  *   o[row, :]  = bf16(out_scale * sum_s w_s o_part[row, s, :] / sum_s w_s)
  *   lse[row]   = M + log2 sum_s w_s            (when lse is non-NULL)
- * with s in increasing order; a row whose partials are all -inf gets o = 0 and
+ * in a fixed association (each column sums its terms in increasing s; sum_s w_s
+ * is 32 lane-strided partial sums joined by a butterfly), so the result does not
+ * vary from call to call; a row whose partials are all -inf gets o = 0 and
  * lse = -inf.  o_part fp32 [rows, num_splits, d_v] (normalized partials),
  * lse_part fp32 [rows, num_splits] base 2, o bf16 [rows, d_v]; d_v a multiple
  * of 8, num_splits in [1, MLA_MAX_SPLITS]; all 16-byte aligned.
@@ -212,7 +219,7 @@ int mla_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
  */
 int mla_plan_force_splits(mla_plan_t* plan, int32_t num_splits);
 
-/* Zero the workspace's error word (enqueued on `stream`). */
+/* Zero the workspace header, which holds the error word (enqueued on `stream`). */
 int mla_workspace_reset(void* workspace, void* stream);
 
 /*

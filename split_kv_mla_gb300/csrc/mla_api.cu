@@ -61,13 +61,12 @@ int64_t workspace_for(int64_t items, int ns, int d_v)
     return bytes;
 }
 
-// Split count for `ctas_per_split` CTAs per split, `keys` keys per request and
-// `items` output rows (row x head) in the call.
-int32_t gb300_splits(int64_t ctas_per_split, int64_t keys, int64_t items, int32_t d_v,
-                     int32_t sm_count)
+// Split count for `tiles` (request, head block) tiles, `keys` keys per
+// request and `items` output rows (row x head) in the call.
+int32_t gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v, int32_t sm_count)
 {
     const int64_t blocks = ceil_div(keys > 0 ? keys : 1, kBlockN);
-    const int64_t ctas = ctas_per_split > 0 ? ctas_per_split : 1;
+    const int64_t ctas = tiles > 0 ? tiles : 1;
     const int64_t max_ns = blocks < MLA_MAX_SPLITS ? blocks : MLA_MAX_SPLITS;
     double best = 0.0;
     int32_t best_ns = 1;
@@ -151,11 +150,12 @@ void carve(const mla_plan_t* plan, void* ws, int64_t items, SplitArgs* a)
     }
 }
 
+bool variant_ok(const mla_plan_t* plan) { return plan->variant == kVariantTc; }
+
 int run(const mla_plan_t* plan, SplitArgs& a, int64_t items, cudaStream_t stream,
         bool with_reduce)
 {
-    cudaError_t e = plan->variant == kVariantTc ? launch_split_tc(a, *plan, stream)
-                                                : launch_split_simt(a, *plan, stream);
+    cudaError_t e = launch_split_tc(a, *plan, stream);
     if (e != cudaSuccess) return MLA_ERR_LAUNCH_FAILED;
     if (with_reduce && plan->num_splits > 1) {
         e = launch_splitk_reduce(a.o_part, a.lse_part, items, plan->num_splits, plan->d_v,
@@ -246,7 +246,7 @@ static int dense_call(const mla_plan_t* plan, const void* q_lat, const void* q_p
     if (!plan) return MLA_ERR_INVALID_ARG;
     if (plan->batch != batch || plan->q_len != q_len || plan->num_heads != num_heads ||
         plan->d_v != kDenseDv || plan->d_rope != kDenseDr ||
-        (plan->variant != kVariantSimt && plan->variant != kVariantTc) ||
+        !variant_ok(plan) ||
         plan->num_splits < 1 || plan->num_splits > MLA_MAX_SPLITS)
         return MLA_ERR_INVALID_ARG;
     if (batch == 0) return MLA_OK;
@@ -297,7 +297,7 @@ static int sparse_call(const mla_plan_t* plan, const void* q_nope, const void* q
     if (!plan) return MLA_ERR_INVALID_ARG;
     if (plan->batch != num_tokens || plan->q_len != 1 || plan->num_heads != num_heads ||
         plan->d_v != kSparseDv || plan->d_rope != kSparseDr ||
-        (plan->variant != kVariantSimt && plan->variant != kVariantTc) ||
+        !variant_ok(plan) ||
         plan->total_keys != (int64_t)num_tokens * topk || plan->num_splits < 1 ||
         plan->num_splits > MLA_MAX_SPLITS)
         return MLA_ERR_INVALID_ARG;
@@ -427,7 +427,7 @@ int mla_plan_force_splits(mla_plan_t* plan, int32_t num_splits)
 int mla_workspace_reset(void* workspace, void* stream)
 {
     if (!workspace) return MLA_ERR_INVALID_ARG;
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t),
+    cudaError_t e = cudaMemsetAsync(workspace, 0, MLA_WORKSPACE_HEADER_BYTES,
                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

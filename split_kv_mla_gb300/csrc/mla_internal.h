@@ -32,13 +32,12 @@ struct SplitArgs {
     int sparse;
 };
 
-// Kernel variants (mla_plan_t::variant).
+// Kernel variants (mla_plan_t::variant).  Value 1 belonged to a CUDA-core
+// bring-up kernel that the tcgen05 kernel replaced; it is rejected.
 enum Variant : int32_t {
-    kVariantSimt = 1,   // CUDA-core split kernel
-    kVariantTc = 2,     // tcgen05 + TMA split kernel
+    kVariantTc = 2,   // tcgen05 + TMA split kernel, then the split-K reduce kernel
 };
 
-cudaError_t launch_split_simt(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream);
 cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
                                  int32_t num_splits, int32_t d_v, float out_scale,

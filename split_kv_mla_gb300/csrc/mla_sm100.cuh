@@ -124,26 +124,6 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// ---- cp.async ----------------------------------------------------------------------------------
-
-// 16-byte global -> shared copy through L2 only.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit()
-{
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Wait until at most n of this thread's committed groups are still pending.
-template <int n>
-__device__ __forceinline__ void cp_async_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
-}
-
 // ---- TMA ---------------------------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap)
@@ -310,16 +290,40 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi)
     return r;
 }
 
-// Packed e4m3x2 -> two fp32 (exact).
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v)
+// Packed e4m3x2 -> two fp32 (exact), with integer and fp32-multiply ops only
+// (no conversion-pipe instructions).  An e4m3fn byte is 1 sign, 4 exponent
+// (bias 7) and 3 mantissa bits; placing its 7 magnitude bits at fp32 bits 20..26
+// gives an fp32 (normal, or subnormal for exponent 0) equal to the byte's value
+// times 2^-120, so one multiply by 2^120 restores it exactly.  The NaN code is
+// never produced by the satfinite conversion above and is not handled.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t v)
 {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
-    float lo, hi;
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h2));
-    return make_float2(lo, hi);
+    const uint32_t lo = ((v & 0x7fu) << 20) | ((v & 0x80u) << 24);
+    const uint32_t hi = ((v & 0x7f00u) << 12) | ((v & 0x8000u) << 16);
+    const float k = 1.329227995784916e+36f;   // 2^120
+    return make_float2(__uint_as_float(lo) * k, __uint_as_float(hi) * k);
+}
+
+// ---- bulk shared -> global stores ---------------------------------------------------------
+
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from shared
+// to global memory with the TMA engine, in this thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(gdst)), "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until this thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 }  // namespace sm100

@@ -104,7 +104,9 @@ struct Misc {
     alignas(16) float cq[32];   // per query row: raw dot -> base-2 logit
     int win[32];        // per query row: keys at positions < win are visible
     float red[4][32];   // cross-warp reduction scratch
-    float fin[2][32];   // epilogue: 1 / lt and the base-2 LSE per row
+    float red2[4][32];  // second reduction scratch (epilogue: the lt sums)
+    alignas(16) float fin[2][32];   // epilogue: 1 / lt and the base-2 LSE per row
+    long long row_item[32];   // epilogue: output row (request row x head) per query row, -1 if none
 };
 
 template <int N, bool SPARSE>
@@ -112,6 +114,7 @@ constexpr int smem_bytes()
 {
     return Cfg<N, SPARSE>::kOffMisc + (int)sizeof(Misc);
 }
+
 
 // Byte offset of column c (0 <= c < row width) of operand row `row` in a tile
 // of `rows` rows laid out as four 128B-swizzled 128-column chunks followed by
@@ -158,9 +161,9 @@ __device__ __forceinline__ int q_shift(float amax)
 __device__ __forceinline__ float2 split_pair(float a, float b, uint16_t& hi, uint16_t& lo)
 {
     hi = f32x2_to_e4m3x2(a, b);
-    const float2 h = e4m3x2_to_f32x2(hi);
+    const float2 h = e4m3x2_to_f32x2((uint32_t)hi);
     lo = f32x2_to_e4m3x2(a - h.x, b - h.y);
-    const float2 l = e4m3x2_to_f32x2(lo);
+    const float2 l = e4m3x2_to_f32x2((uint32_t)lo);
     return make_float2(h.x + l.x, h.y + l.y);
 }
 
@@ -260,6 +263,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hb = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+    // Let a programmatic dependent (the split-K reduce) be scheduled as soon as
+    // every CTA of this grid has started; it waits for this grid's completion
+    // before reading anything.
+    asm volatile("griddepcontrol.launch_dependents;");
     const int rows_in_req = a.q_len * a.num_heads;
 
     // ---- the request's key list and this split's range --------------------------------
@@ -706,34 +713,55 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.p_full[st]);
-            // running sums of this warp's 32 keys: lane ends up with row my_row
+            // Running sums of this warp's 32 keys (lane ends up with row my_row).
+            // The empty asm keeps the compiler from scheduling these shuffles
+            // ahead of the P hand-off above, where they would delay the MMA.
+#pragma unroll
+            for (int n = 0; n < N; ++n) asm volatile("" : "+f"(s[n]), "+f"(pt[n]));
             l_acc += warp_transpose_reduce<N, false>(s, lane);
             lt_acc += warp_transpose_reduce<N, false>(pt, lane);
         }
 
         // ---- epilogue ------------------------------------------------------------------------
-        // row sums over all 128 keys, then 1/lt and the LSE per row
-        if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = l_acc;
+        // Row sums over all 128 keys -> 1/lt and the base-2 LSE per row, and each
+        // row's output index; then O^T leaves TMEM already normalised (times
+        // 1/lt, and kv_scale into bf16 for a single split) into the idle KV
+        // stages, and one bulk TMA store per row writes it out.
+        if ((lane % kLanesPerRow) == 0) {
+            ms.red[sw][my_row] = l_acc;
+            ms.red2[sw][my_row] = lt_acc;
+        }
         softmax_bar();
-        float lsum = 0.f;
-        if (ti < N) lsum = ms.red[0][ti] + ms.red[1][ti] + ms.red[2][ti] + ms.red[3][ti];
-        softmax_bar();
-        if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = lt_acc;
-        softmax_bar();
+        const int ns = a.num_splits;
         if (ti < N) {
-            const float ltsum = ms.red[0][ti] + ms.red[1][ti] + ms.red[2][ti] + ms.red[3][ti];
+            const float lsum = ms.red[0][ti] + ms.red[1][ti] + ms.red[2][ti] + ms.red[3][ti];
+            const float ltsum = ms.red2[0][ti] + ms.red2[1][ti] + ms.red2[2][ti] + ms.red2[3][ti];
             float mr = 0.f;
 #pragma unroll
             for (int n = 0; n < N; ++n)
                 if (n == ti) mr = m_ref[n];
             ms.fin[0][ti] = ltsum > 0.f ? 1.f / ltsum : 0.f;
             ms.fin[1][ti] = lsum > 0.f ? mr + log2f(lsum) - kShift : -CUDART_INF_F;
+            const int idx = hb * N + ti;
+            ms.row_item[ti] = idx < rows_in_req
+                ? ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads
+                : -1;
         }
         const bool have_o = alive && nblk > 0 && warp_wait(&ms.o_done, 0, abort_flag);
         if (have_o) tc_fence_after();
-        // O^T (+ hi/lo halves) -> ostage[n][d] fp32 in the now idle KV stages, then
-        // one compact cooperative loop writes normalized rows with 16-byte stores.
-        float* ostage = reinterpret_cast<float*>(smem + C::kOffStage);
+        softmax_bar();
+        float inv[N];
+#pragma unroll
+        for (int g = 0; g < N / 4; ++g) {
+            const float4 v = reinterpret_cast<const float4*>(ms.fin[0])[g];
+            inv[4 * g] = v.x;
+            inv[4 * g + 1] = v.y;
+            inv[4 * g + 2] = v.z;
+            inv[4 * g + 3] = v.w;
+        }
+        const bool final_rows = ns == 1;
+        float* ostage = reinterpret_cast<float*>(smem + C::kOffStage);              // fp32 [N][512]
+        uint16_t* ostage16 = reinterpret_cast<uint16_t*>(smem + C::kOffStage);      // bf16 [N][512]
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             float o[N];
@@ -743,46 +771,30 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
                 for (int n = 0; n < N; ++n) o[n] = 0.f;
             }
+            if (final_rows) {
 #pragma unroll
-            for (int n = 0; n < N; ++n) ostage[n * 512 + c * 128 + ti] = o[n];
-        }
-        softmax_bar();
-        const int ns = a.num_splits;
-        constexpr int kQuads = C::kDv / 4;
-#pragma unroll 1
-        for (int it = ti; it < N * kQuads; it += 128) {
-            const int n = it / kQuads;
-            const int d = (it % kQuads) * 4;
-            const int idx = hb * N + n;
-            if (idx >= rows_in_req) continue;
-            const int64_t item =
-                ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads;
-            const float inv = ms.fin[0][n];
-            const float4 v = *reinterpret_cast<const float4*>(ostage + n * 512 + d);
-            if (ns == 1) {
-                const float f = inv * a.out_scale;
-                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * f, v.y * f);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * f, v.w * f);
-                uint2 pk;
-                pk.x = *reinterpret_cast<uint32_t*>(&lo);
-                pk.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(a.o + item * C::kDv + d) = pk;
+                for (int n = 0; n < N; ++n)
+                    ostage16[n * 512 + c * 128 + ti] =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(o[n] * (inv[n] * a.out_scale)));
             } else {
-                *reinterpret_cast<float4*>(a.o_part + (item * ns + split) * C::kDv + d) =
-                    make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+#pragma unroll
+                for (int n = 0; n < N; ++n) ostage[n * 512 + c * 128 + ti] = o[n] * inv[n];
             }
         }
+        fence_proxy_async_smem();
+        softmax_bar();
         if (ti < N) {
-            const int idx = hb * N + ti;
-            if (idx < rows_in_req) {
-                const int64_t item =
-                    ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads;
-                const float lse2 = ms.fin[1][ti];
-                if (ns == 1) {
-                    if (a.lse) a.lse[item] = lse2;
+            const long long item = ms.row_item[ti];
+            if (item >= 0) {
+                if (final_rows) {
+                    bulk_store(a.o + item * C::kDv, ostage16 + ti * 512, C::kDv * 2);
+                    if (a.lse) a.lse[item] = ms.fin[1][ti];
                 } else {
-                    a.lse_part[item * ns + split] = lse2;
+                    bulk_store(a.o_part + (item * ns + split) * C::kDv, ostage + ti * 512, C::kDv * 4);
+                    a.lse_part[item * ns + split] = ms.fin[1][ti];
                 }
+                bulk_commit();
+                bulk_wait_read();
             }
         }
         if ((!alive || *abort_flag) && lane == 0) atomicOr(a.err, MLA_DEVERR_TIMEOUT);

@@ -82,7 +82,7 @@ def test_dense_plan_invariants(lib, batch, q_len, heads, keys):
     assert (p.batch, p.q_len, p.num_heads, p.d_v, p.d_rope, p.total_keys) == (
         batch, q_len, heads, 512, 64, keys)
     items = batch * q_len * heads
-    expect = 256
+    expect = mla.MLA_WORKSPACE_HEADER_BYTES
     if p.num_splits > 1:
         def up(x):
             return -(-x // 256) * 256
@@ -100,7 +100,8 @@ def test_force_splits_recomputes_grid_and_workspace(lib):
         assert q.num_splits == ns and q.grid_y == ns
         items = 8 * 16
         up = lambda x: -(-x // 256) * 256  # noqa: E731
-        expect = 256 + ((up(items * ns * 512 * 4) + up(items * ns * 4)) if ns > 1 else 0)
+        expect = mla.MLA_WORKSPACE_HEADER_BYTES + (
+            (up(items * ns * 512 * 4) + up(items * ns * 4)) if ns > 1 else 0)
         assert q.workspace_bytes == expect
     with pytest.raises(mla.MlaError):
         mla.mla_plan_force_splits(p, 0)
@@ -156,3 +157,19 @@ def test_reduce_argument_checks(lib):
     assert lib.mla_splitk_reduce(P(0x1000), P(0x1000), 4, 2, 12, 1.0, P(0x1000), None, None) == -2
     assert lib.mla_splitk_reduce(P(0x1004), P(0x1000), 4, 2, 512, 1.0, P(0x1000), None, None) == -3
     assert lib.mla_splitk_reduce(None, None, 0, 2, 512, 1.0, None, None, None) == 0
+
+
+def test_plans_use_the_tcgen05_variant(lib):
+    for batch, q_len, heads, keys in [(8, 1, 16, 8 * 8192), (1, 1, 16, 131072),
+                                      (64, 1, 128, 1081344), (3, 7, 5, 10)]:
+        p = mla.mla_decode_plan(batch, q_len, heads, keys, 152)
+        assert p.variant == 2
+        assert mla.mla_plan_force_splits(p, 7).variant == 2
+    assert mla.mla_sparse_decode_plan(2, 128, 1024, 152).variant == 2
+
+
+def test_decode_rejects_unknown_variant(lib):
+    for variant in (0, 1, 3, 4):
+        plan = mla.mla_plan_force_splits(mla.mla_decode_plan(1, 1, 16, 4096, 152), 4)
+        plan.variant = variant
+        assert _call_decode(lib, plan, ws_bytes=plan.workspace_bytes) == -1, variant

@@ -21,15 +21,18 @@
 //   precise as rounding p to bf16).  hi and lo are stacked along N (2N MMA
 //   columns), so the big operand is read from shared memory once per MMA.
 //   kv_scale and the powers of two are folded into the logit and output scales.
-// * Warp roles.  Warps 0-3 gather the block's 128 rows with TMA tile::gather4
+// * Warp roles.  Warps 0-6 gather the block's 128 rows with TMA tile::gather4
 //   (four slots per instruction; 128-byte latent boxes land 128B-swizzled, the
 //   64-byte RoPE box 64B-swizzled: exactly the K-major operand layout) into a
-//   two-stage ring, 32 rows per warp; warp 4 issues the tcgen05.mma
-//   (kind::f8f6f4, fp32 accumulators in TMEM) and commits to mbarriers; warps 5-8
-//   own one TMEM lane (= one key) each and run the online base-2 softmax.
-//   Measured on GB300, random 576-byte rows gather at ~4.8 TB/s when four warps
-//   issue gather4 (one issuing warp: ~2 TB/s); TMA keeps the bytes off the SM's
-//   load/store path, which the softmax warps' shared loads and shuffles use.
+//   two-stage ring, the block's 160 copies dealt out over the seven warps; warp 7
+//   issues the tcgen05.mma (kind::f8f6f4, fp32 accumulators in TMEM) and commits
+//   to mbarriers; warps 8-11 own one TMEM lane (= one key) each and run the online
+//   base-2 softmax.  Measured on GB300, a warp issues one gather4 about every 100
+//   cycles, so a block's issue time falls with the number of issuing warps (per
+//   SM, random 576-byte rows gather at ~38 GB/s from four warps, ~54 GB/s from
+//   eight); twelve warps keep the register budget of nine (three warps per SM
+//   sub-partition either way).  TMA keeps the bytes off the SM's load/store path,
+//   which the softmax warps' shared loads and shuffles use.
 // * Lazy rescaling.  A block only recomputes the running maxima when some logit
 //   exceeds them by more than kTau; otherwise p = 2^(s - m) stays below 2^kTau.
 //   The decision is one hardware barrier-reduction (bar.red.or) of the four
@@ -57,14 +60,14 @@ namespace {
 using namespace sm100;
 
 constexpr int kBlockN = 128;          // keys per block (MMA M)
-constexpr int kThreads = 288;         // warps 0-3 gather, warp 4 MMA, warps 5-8 softmax
+constexpr int kThreads = 384;         // warps 0-6 gather, warp 7 MMA, warps 8-11 softmax
 constexpr int kWarps = kThreads / 32;
-constexpr int kGatherWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kSoftmaxWarp0 = 5;
+constexpr int kGatherWarps = 7;
+constexpr int kMmaWarp = 7;
+constexpr int kSoftmaxWarp0 = 8;
 constexpr float kTau = 2.f;           // lazy-rescale threshold, base-2 logit units
 constexpr float kShift = 6.f;         // p is fed as p * 2^kShift: at most 2^(kTau + kShift) = 256
-constexpr int kQWarps = kWarps - kMmaWarp;   // warps 4-8 split the query tile
+constexpr int kQWarps = kWarps - kMmaWarp;   // warps 7-11 split the query tile
 constexpr uint32_t kQBar = 2;                // their named barrier (id 1 is the softmax one)
 constexpr uint32_t kGatherSleepNs = 128;
 constexpr uint32_t kMmaSleepNs = 32;
@@ -312,84 +315,93 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const uint32_t tmem = ms.tmem_base;
     const uint32_t smem_base = smem_u32(smem);
 
-    // ---- gather helpers (warps 0-3, 32 rows = 8 four-row groups each) ---------------------------
-    const int32_t* list = a.kv_indices + base;
-    const int grow = warp * 32 + lane;   // a gather lane's row of every block
-    // Slot of this lane's row of block j; masked keys read pool row 0 (finite
-    // bytes; their p is 0).
-    auto raw_slot = [&](int j) -> int32_t {   // the index itself (-1 past the split)
-        const int kb = k0 + j * kBlockN;
-        const int nk = min(kBlockN, k1 - kb);
-        return grow < nk ? __ldg(list + kb + grow) : -1;
-    };
-    auto check_slot = [&](int j, int32_t v, int& ok) -> int32_t {
-        const int kb = k0 + j * kBlockN;
-        const int nk = min(kBlockN, k1 - kb);
-        ok = 0;
-        if (grow < nk) {
-            if (v >= 0 && (int64_t)v < a.pool_rows) ok = 1;
-            else if (!(SPARSE && v < 0)) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
-        }
-        return ok ? v : 0;
-    };
-    auto load_slot = [&](int j, int& ok) -> int32_t { return check_slot(j, raw_slot(j), ok); };
-    // Block j into stage j & 1: the warp's 8 groups x (4 latent boxes + RoPE box),
-    // spread over its lanes; every block loads all 128 rows.
+    // ---- gather helpers (warps 0-6) ---------------------------------------------------------
+    // A block is 32 four-row groups x kBoxes boxes (the four 128-byte latent
+    // chunks, then the 64-byte RoPE chunk): kItems tile::gather4 copies, dealt
+    // out kItemsPerWarp per warp and one per lane.  TMA issue is serial within
+    // a warp, so spreading the copies over seven warps shortens a block's issue.
     constexpr int kBoxes = C::kRope ? 5 : 4;
-    auto issue = [&](int j, int32_t sl, int ok) {
-        const int st = j & 1;
-        ms.kvalid[st][grow] = ok;
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&ms.kv_full[st], 32u * kWidth);
-        __syncwarp();
-        uint8_t* stage = smem + C::kOffStage + st * C::kStageBytes;
-        // item = (group, box); lane handles items lane and lane + 32.  Every
-        // shuffle runs on all 32 lanes (source lanes clamped for idle items);
-        // only the copies themselves are predicated.
+    constexpr int kItems = 32 * kBoxes;
+    constexpr int kItemsPerWarp = (kItems + kGatherWarps - 1) / kGatherWarps;
+    static_assert(kItemsPerWarp <= 32, "one copy per lane");
+    const int32_t* list = a.kv_indices + base;
+    const int my_item = warp * kItemsPerWarp + lane;
+    const bool item_on = warp < kGatherWarps && lane < kItemsPerWarp && my_item < kItems;
+    const int my_group = item_on ? my_item / kBoxes : 0;   // rows 4 g .. 4 g + 3
+    const int my_box = item_on ? my_item % kBoxes : 0;
+    const bool owns_group = item_on && my_box == 0;        // checks the slots, writes kvalid
+    struct Slots { int32_t v[4]; };
+    // The four indices of this lane's group in block j (-1 past the split).
+    auto raw_slots = [&](int j) -> Slots {
+        Slots r;
+        const int kb = k0 + j * kBlockN;
+        const int nk = min(kBlockN, k1 - kb);
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int item = lane + 32 * pass;
-            const bool active = item < 8 * kBoxes;
-            const int gl = active ? item / kBoxes : 0;
-            const int c = active ? item % kBoxes : 0;
-            const int32_t r0 = __shfl_sync(0xffffffffu, sl, 4 * gl);
-            const int32_t r1 = __shfl_sync(0xffffffffu, sl, 4 * gl + 1);
-            const int32_t r2 = __shfl_sync(0xffffffffu, sl, 4 * gl + 2);
-            const int32_t r3 = __shfl_sync(0xffffffffu, sl, 4 * gl + 3);
-            if (active) {
-                const int g = warp * 8 + gl;
-                if (c < 4)
-                    tma_gather4(stage + c * C::kLatChunkBytes + g * 512, &tm_lat, c * 128,
-                                r0, r1, r2, r3, &ms.kv_full[st]);
-                else
-                    tma_gather4(stage + 4 * C::kLatChunkBytes + g * 256, &tm_rope, 512,
-                                r0, r1, r2, r3, &ms.kv_full[st]);
+        for (int i = 0; i < 4; ++i) {
+            const int row = 4 * my_group + i;
+            r.v[i] = (item_on && row < nk) ? __ldg(list + kb + row) : -1;
+        }
+        return r;
+    };
+    // Slots to gather (masked or invalid keys read pool row 0: finite bytes,
+    // p = 0) and the validity bits of the four keys.
+    auto check_slots = [&](int j, Slots r, int (&ok)[4]) -> Slots {
+        const int kb = k0 + j * kBlockN;
+        const int nk = min(kBlockN, k1 - kb);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int32_t v = r.v[i];
+            ok[i] = 0;
+            if (4 * my_group + i < nk) {
+                if (v >= 0 && (int64_t)v < a.pool_rows) ok[i] = 1;
+                else if (owns_group && !(SPARSE && v < 0)) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
             }
+            r.v[i] = ok[i] ? v : 0;
+        }
+        return r;
+    };
+    // bytes this warp's copies bring per block
+    const uint32_t warp_bytes = __reduce_add_sync(
+        0xffffffffu, item_on ? (my_box < 4 ? 512u : 256u) : 0u);
+    // Block j into stage j & 1.
+    auto issue = [&](int j, const Slots& sl, const int (&ok)[4]) {
+        const int st = j & 1;
+        if (owns_group) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ms.kvalid[st][4 * my_group + i] = ok[i];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&ms.kv_full[st], warp_bytes);
+        __syncwarp();
+        if (item_on) {
+            uint8_t* stage = smem + C::kOffStage + st * C::kStageBytes;
+            if (my_box < 4)
+                tma_gather4(stage + my_box * C::kLatChunkBytes + my_group * 512, &tm_lat,
+                            my_box * 128, sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
+            else
+                tma_gather4(stage + 4 * C::kLatChunkBytes + my_group * 256, &tm_rope, 512,
+                            sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
         }
     };
-    int gok = 0;
-    int32_t gnext = 0;
+    int gok[4] = {0, 0, 0, 0};
+    Slots gnext{};
     if (warp < kGatherWarps && nblk > 0) {
         // start the first two blocks before anything else
         if (lane == 0) {
             tma_prefetch_desc(&tm_lat);
             if (C::kRope) tma_prefetch_desc(&tm_rope);
         }
-        // the three index loads are in flight together
-        const int32_t v0 = raw_slot(0);
-        const int32_t v1 = nblk > 1 ? raw_slot(1) : -1;
-        const int32_t v2 = nblk > 2 ? raw_slot(2) : -1;
-        int ok;
-        int32_t sl = check_slot(0, v0, ok);
-        issue(0, sl, ok);
-        if (nblk > 1) {
-            sl = check_slot(1, v1, ok);
-            issue(1, sl, ok);
-        }
-        if (nblk > 2) gnext = check_slot(2, v2, gok);
+        // the index loads of blocks 0-2 are in flight together
+        const Slots r0 = raw_slots(0);
+        const Slots r1 = nblk > 1 ? raw_slots(1) : Slots{{-1, -1, -1, -1}};
+        const Slots r2 = nblk > 2 ? raw_slots(2) : Slots{{-1, -1, -1, -1}};
+        int ok[4];
+        issue(0, check_slots(0, r0, ok), ok);
+        if (nblk > 1) issue(1, check_slots(1, r1, ok), ok);
+        if (nblk > 2) gnext = check_slots(2, r2, gok);
     }
 
-    // ---- the query tile: one warp per row, warps 4-8 ---------------------------------------------
+    // ---- the query tile: one warp per row, warps 7-11 --------------------------------------------
     // q is scaled by 2^sh so that max |q| is in [128, 256), then split into e4m3
     // hi (tile rows 0..N-1) and lo (rows N..2N-1).  The gather warps go on
     // loading meanwhile; the MMA warp waits for the tile at the warps' barrier.
@@ -473,7 +485,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 break;
             issue(j, gnext, gok);
             issued = j + 1;
-            if (j + 1 < nblk) gnext = load_slot(j + 1, gok);
+            if (j + 1 < nblk) gnext = check_slots(j + 1, raw_slots(j + 1), gok);
         }
         // Never leave the CTA with loads in flight: the last two issued blocks
         // (earlier ones were consumed before their stage was reused) must land.
@@ -565,7 +577,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
         __syncwarp();
     } else {
-        // ================= softmax + epilogue (warps 5..8) =====================================
+        // ================= softmax + epilogue (warps 8..11) ====================================
         const int sw = warp - kSoftmaxWarp0;      // 0..3
         const int quad = warp & 3;                // TMEM lane quadrant of this warp
         const int ti = quad * 32 + lane;          // key within a block == TMEM lane

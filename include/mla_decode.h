@@ -96,6 +96,11 @@ typedef struct {
     int64_t workspace_bytes; /* bytes of device workspace the call needs */
     int32_t batch, q_len, num_heads, d_v, d_rope, sm_count;
     int64_t total_keys;      /* dense: kv_indices length; sparse: tokens * topk */
+    int32_t kv_share;        /* head blocks (CTAs) that share each gathered KV block
+                                through a thread-block cluster and TMA multicast:
+                                1, 2, 4 or 8, dividing head_blocks (1 when
+                                rows_per_cta is 16); results do not depend on it */
+    int32_t reserved;        /* 0 */
 } mla_plan_t;
 
 /*

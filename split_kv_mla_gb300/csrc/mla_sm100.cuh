@@ -144,6 +144,38 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
+// tma_gather4 delivered to the same shared-memory offset in every CTA of the
+// cluster named by cta_mask; each destination CTA's mbarrier at bar's offset
+// receives the bytes that land there.
+__device__ __forceinline__ void tma_gather4_multicast(void* dst, const void* tmap, int32_t x,
+                                                      int32_t r0, int32_t r1, int32_t r2,
+                                                      int32_t r3, uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1),
+          "r"(r2), "r"(r3), "r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
+}
+
+// ---- thread-block clusters ---------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Barrier of every thread of every CTA in the cluster, with release/acquire
+// ordering of shared-memory operations.  All threads of each CTA must reach it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---- tensor memory ---------------------------------------------------------------------------
 
 // Allocate ncols (power of two >= 32) TMEM columns; the base address is
@@ -276,6 +308,17 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
         ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+// The same commit, arriving on the mbarrier at this offset in every CTA of the
+// cluster named by cta_mask.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(cta_mask)
         : "memory");
 }
 

@@ -100,7 +100,7 @@ struct Cfg {
 };
 
 struct Misc {
-    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], o_done;
+    uint64_t kv_full[2], kv_empty[2], pv_done[2], s_full[2], s_free[2], p_full[2], o_done;
     uint32_t tmem_base;
     int abort;
     int kvalid[2][kBlockN];
@@ -252,7 +252,7 @@ __device__ __forceinline__ void load_cols(uint32_t taddr, float (&s)[N])
     }
 }
 
-template <int N, bool SPARSE>
+template <int N, bool SPARSE, int CH>
 __global__ void __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 const __grid_constant__ CUtensorMap tm_rope, const SplitArgs a)
@@ -293,10 +293,17 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const int nblk = (k1 - k0 + kBlockN - 1) / kBlockN;
 
     // ---- barriers and TMEM ----------------------------------------------------------------
+    // With CH > 1 the CH head blocks of one (request, split) form a cluster that
+    // shares every gathered block: rank r issues the r-th share of the block's
+    // copies and multicasts them to all CH CTAs, so each KV byte leaves memory
+    // once.  A stage is refilled only when every CTA of the cluster has finished
+    // its P.V on it (kv_empty collects one arrival per CTA); pv_done is the
+    // CTA's own P.V completion.
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.kv_full[i], kGatherWarps);   // one arrival per gather warp
-            mbar_init(&ms.kv_empty[i], 1);
+            mbar_init(&ms.kv_empty[i], CH);
+            mbar_init(&ms.pv_done[i], 1);
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.s_free[i], 4);
             mbar_init(&ms.p_full[i], 4);
@@ -310,28 +317,40 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if (CH > 1)
+        cluster_sync();   // peers' barriers are initialised before any multicast lands
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms.tmem_base;
     const uint32_t smem_base = smem_u32(smem);
+    const int rank = CH > 1 ? (int)cluster_ctarank() : 0;
+    constexpr uint16_t kClusterMask = (uint16_t)((1u << CH) - 1u);
 
     // ---- gather helpers (warps 0-6) ---------------------------------------------------------
     // A block is 32 four-row groups x kBoxes boxes (the four 128-byte latent
-    // chunks, then the 64-byte RoPE chunk): kItems tile::gather4 copies, dealt
-    // out kItemsPerWarp per warp and one per lane.  TMA issue is serial within
-    // a warp, so spreading the copies over seven warps shortens a block's issue.
+    // chunks, then the 64-byte RoPE chunk): kItems tile::gather4 copies, of
+    // which this CTA issues its cluster rank's share (all of them when CH == 1),
+    // dealt out kItemsPerWarp per warp and one per lane.  TMA issue is serial
+    // within a warp, so spreading the copies over seven warps shortens a
+    // block's issue.  The key-validity bits of all 128 rows are computed by every
+    // CTA itself (lanes of warps 0-3, one row each).
     constexpr int kBoxes = C::kRope ? 5 : 4;
     constexpr int kItems = 32 * kBoxes;
-    constexpr int kItemsPerWarp = (kItems + kGatherWarps - 1) / kGatherWarps;
+    static_assert(kItems % CH == 0, "copies split evenly over the cluster");
+    constexpr int kItemsCta = kItems / CH;
+    constexpr int kItemsPerWarp = (kItemsCta + kGatherWarps - 1) / kGatherWarps;
     static_assert(kItemsPerWarp <= 32, "one copy per lane");
     const int32_t* list = a.kv_indices + base;
-    const int my_item = warp * kItemsPerWarp + lane;
-    const bool item_on = warp < kGatherWarps && lane < kItemsPerWarp && my_item < kItems;
+    const int cta_item = warp * kItemsPerWarp + lane;
+    const bool item_on = warp < kGatherWarps && lane < kItemsPerWarp && cta_item < kItemsCta;
+    const int my_item = rank * kItemsCta + cta_item;
     const int my_group = item_on ? my_item / kBoxes : 0;   // rows 4 g .. 4 g + 3
     const int my_box = item_on ? my_item % kBoxes : 0;
-    const bool owns_group = item_on && my_box == 0;        // checks the slots, writes kvalid
+    const bool row_lane = tid < kBlockN;                   // warps 0-3: row tid's validity
     struct Slots { int32_t v[4]; };
-    // The four indices of this lane's group in block j (-1 past the split).
+    // The four indices of this lane's group in block j (-1 past the split),
+    // and row tid's index.
     auto raw_slots = [&](int j) -> Slots {
         Slots r;
         const int kb = k0 + j * kBlockN;
@@ -343,48 +362,55 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
         return r;
     };
-    // Slots to gather (masked or invalid keys read pool row 0: finite bytes,
-    // p = 0) and the validity bits of the four keys.
-    auto check_slots = [&](int j, Slots r, int (&ok)[4]) -> Slots {
+    auto raw_row = [&](int j) -> int32_t {
         const int kb = k0 + j * kBlockN;
         const int nk = min(kBlockN, k1 - kb);
+        return (row_lane && tid < nk) ? __ldg(list + kb + tid) : -1;
+    };
+    auto slot_ok = [&](int32_t v) { return v >= 0 && (int64_t)v < a.pool_rows; };
+    // Slots to gather: masked or invalid keys read pool row 0 (finite bytes, p = 0).
+    auto fix_slots = [&](Slots r) -> Slots {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int32_t v = r.v[i];
-            ok[i] = 0;
-            if (4 * my_group + i < nk) {
-                if (v >= 0 && (int64_t)v < a.pool_rows) ok[i] = 1;
-                else if (owns_group && !(SPARSE && v < 0)) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
-            }
-            r.v[i] = ok[i] ? v : 0;
-        }
+        for (int i = 0; i < 4; ++i) r.v[i] = slot_ok(r.v[i]) ? r.v[i] : 0;
         return r;
     };
-    // bytes this warp's copies bring per block
-    const uint32_t warp_bytes = __reduce_add_sync(
-        0xffffffffu, item_on ? (my_box < 4 ? 512u : 256u) : 0u);
-    // Block j into stage j & 1.
-    auto issue = [&](int j, const Slots& sl, const int (&ok)[4]) {
+    // Validity of row tid (a dense slot out of range is reported, not read).
+    auto row_valid = [&](int j, int32_t v) -> int {
+        const int kb = k0 + j * kBlockN;
+        const int nk = min(kBlockN, k1 - kb);
+        if (!row_lane || tid >= nk) return 0;
+        if (slot_ok(v)) return 1;
+        if (!(SPARSE && v < 0) && rank == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
+        return 0;
+    };
+    // Block j into stage j & 1 (of every CTA of the cluster).  Warp 0 announces
+    // the whole stage's bytes, which arrive from this CTA's and its peers' copies.
+    auto issue = [&](int j, const Slots& sl, int rowok) {
         const int st = j & 1;
-        if (owns_group) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ms.kvalid[st][4 * my_group + i] = ok[i];
-        }
+        if (row_lane) ms.kvalid[st][tid] = rowok;
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&ms.kv_full[st], warp_bytes);
+        if (lane == 0) {
+            if (warp == 0)
+                mbar_arrive_expect_tx(&ms.kv_full[st], (uint32_t)C::kStageBytes);
+            else
+                mbar_arrive(&ms.kv_full[st]);
+        }
         __syncwarp();
         if (item_on) {
             uint8_t* stage = smem + C::kOffStage + st * C::kStageBytes;
-            if (my_box < 4)
-                tma_gather4(stage + my_box * C::kLatChunkBytes + my_group * 512, &tm_lat,
-                            my_box * 128, sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
+            uint8_t* dst = my_box < 4 ? stage + my_box * C::kLatChunkBytes + my_group * 512
+                                      : stage + 4 * C::kLatChunkBytes + my_group * 256;
+            const CUtensorMap* map = my_box < 4 ? &tm_lat : &tm_rope;
+            const int x = my_box < 4 ? my_box * 128 : 512;
+            if (CH > 1)
+                tma_gather4_multicast(dst, map, x, sl.v[0], sl.v[1], sl.v[2], sl.v[3],
+                                      &ms.kv_full[st], kClusterMask);
             else
-                tma_gather4(stage + 4 * C::kLatChunkBytes + my_group * 256, &tm_rope, 512,
-                            sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
+                tma_gather4(dst, map, x, sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
         }
     };
-    int gok[4] = {0, 0, 0, 0};
     Slots gnext{};
+    int32_t rnext = -1;
     if (warp < kGatherWarps && nblk > 0) {
         // start the first two blocks before anything else
         if (lane == 0) {
@@ -392,13 +418,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             if (C::kRope) tma_prefetch_desc(&tm_rope);
         }
         // the index loads of blocks 0-2 are in flight together
-        const Slots r0 = raw_slots(0);
-        const Slots r1 = nblk > 1 ? raw_slots(1) : Slots{{-1, -1, -1, -1}};
-        const Slots r2 = nblk > 2 ? raw_slots(2) : Slots{{-1, -1, -1, -1}};
-        int ok[4];
-        issue(0, check_slots(0, r0, ok), ok);
-        if (nblk > 1) issue(1, check_slots(1, r1, ok), ok);
-        if (nblk > 2) gnext = check_slots(2, r2, gok);
+        const Slots s0 = raw_slots(0);
+        const int32_t w0 = raw_row(0);
+        const Slots s1 = nblk > 1 ? raw_slots(1) : Slots{{-1, -1, -1, -1}};
+        const int32_t w1 = nblk > 1 ? raw_row(1) : -1;
+        gnext = nblk > 2 ? raw_slots(2) : Slots{{-1, -1, -1, -1}};
+        rnext = nblk > 2 ? raw_row(2) : -1;
+        issue(0, fix_slots(s0), row_valid(0, w0));
+        if (nblk > 1) issue(1, fix_slots(s1), row_valid(1, w1));
     }
 
     // ---- the query tile: one warp per row, warps 7-11 --------------------------------------------
@@ -483,9 +510,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         for (int j = 2; j < nblk; ++j) {
             if (!warp_wait(&ms.kv_empty[j & 1], ((j - 2) >> 1) & 1, abort_flag, kGatherSleepNs))
                 break;
-            issue(j, gnext, gok);
+            issue(j, fix_slots(gnext), row_valid(j, rnext));
             issued = j + 1;
-            if (j + 1 < nblk) gnext = check_slots(j + 1, raw_slots(j + 1), gok);
+            if (j + 1 < nblk) {
+                gnext = raw_slots(j + 1);
+                rnext = raw_row(j + 1);
+            }
         }
         // Never leave the CTA with loads in flight: the last two issued blocks
         // (earlier ones were consumed before their stage was reused) must land.
@@ -523,7 +553,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                 a0 + (uint64_t)((c * C::kLatChunkBytes + kk * 4096) >> 4),
                                 b0 + (uint64_t)((kk * 512) >> 4), id_pv,
                                 (blk > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&ms.kv_empty[st]);
+                umma_commit(&ms.pv_done[st]);
+                // the stage may be refilled once every CTA of the cluster is done
+                // with it (the last two blocks' stages are never refilled)
+                if (CH == 1)
+                    umma_commit(&ms.kv_empty[st]);
+                else if (blk + 2 < nblk)
+                    umma_commit_multicast(&ms.kv_empty[st], kClusterMask);
             };
             auto issue_qk = [&](int blk) {
                 const int st = blk & 1;
@@ -670,7 +706,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 lt_acc *= a_mine;
                 if (rescale && blk > 0) {
                     // O^T holds blocks < blk: wait for the last P.V, then scale its columns.
-                    if (warp_wait(&ms.kv_empty[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag)) {
+                    if (warp_wait(&ms.pv_done[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag)) {
                         tc_fence_after();
 #pragma unroll 1
                         for (int c = 0; c < 4; ++c) {
@@ -692,7 +728,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 }
             }
             // P^T row ti: bytes [0, N) = p_hi, [N, 2N) = p_lo, of p * 2^kShift.
-            if (blk >= 2) warp_wait(&ms.kv_empty[st], ((blk - 2) >> 1) & 1, abort_flag);
+            if (blk >= 2) warp_wait(&ms.pv_done[st], ((blk - 2) >> 1) & 1, abort_flag);
             float pt[N];
             uint32_t hiw[N / 4], low[N / 4];
 #pragma unroll
@@ -813,8 +849,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
 
     // ---- teardown -------------------------------------------------------------------------------
+    // In a cluster no CTA leaves while a peer may still multicast into its
+    // stages or arrive on its barriers.
     tc_fence_before();
-    __syncthreads();
+    if (CH > 1)
+        cluster_sync();
+    else
+        __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -853,7 +894,7 @@ bool make_row_map(CUtensorMap* m, const void* pool, int64_t rows, int row_bytes,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int N, bool SPARSE>
+template <int N, bool SPARSE, int CH>
 cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
                            const mla_plan_t& plan, cudaStream_t stream)
 {
@@ -861,13 +902,37 @@ cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, cons
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(split_tc_kernel<N, SPARSE>,
+        attr = cudaFuncSetAttribute(split_tc_kernel<N, SPARSE, CH>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr != cudaSuccess) return attr;
-    dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-    split_tc_kernel<N, SPARSE><<<grid, kThreads, smem, stream>>>(lat, rope, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid_x, plan.grid_y, plan.grid_z);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute la[1];
+    if (CH > 1) {
+        // the CH head blocks of one (request, split) share every gathered block
+        la[0].id = cudaLaunchAttributeClusterDimension;
+        la[0].val.clusterDim.x = CH;
+        la[0].val.clusterDim.y = 1;
+        la[0].val.clusterDim.z = 1;
+        cfg.attrs = la;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, split_tc_kernel<N, SPARSE, CH>, lat, rope, a);
+}
+
+template <bool SPARSE>
+cudaError_t launch_rows32(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
+                          const mla_plan_t& plan, cudaStream_t stream)
+{
+    switch (plan.kv_share) {
+    case 2: return launch_variant<32, SPARSE, 2>(lat, rope, a, plan, stream);
+    case 4: return launch_variant<32, SPARSE, 4>(lat, rope, a, plan, stream);
+    default: return launch_variant<32, SPARSE, 1>(lat, rope, a, plan, stream);
+    }
 }
 
 }  // namespace
@@ -886,11 +951,11 @@ cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStre
         rope = lat;
     }
     if (a.sparse) {
-        if (plan.rows_per_cta == 16) return launch_variant<16, true>(lat, rope, a, plan, stream);
-        return launch_variant<32, true>(lat, rope, a, plan, stream);
+        if (plan.rows_per_cta == 16) return launch_variant<16, true, 1>(lat, rope, a, plan, stream);
+        return launch_rows32<true>(lat, rope, a, plan, stream);
     }
-    if (plan.rows_per_cta == 16) return launch_variant<16, false>(lat, rope, a, plan, stream);
-    return launch_variant<32, false>(lat, rope, a, plan, stream);
+    if (plan.rows_per_cta == 16) return launch_variant<16, false, 1>(lat, rope, a, plan, stream);
+    return launch_rows32<false>(lat, rope, a, plan, stream);
 }
 
 }  // namespace mla

@@ -46,7 +46,8 @@ class mla_plan_t(ctypes.Structure):
         ("variant", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
         ("batch", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_heads", ctypes.c_int32),
         ("d_v", ctypes.c_int32), ("d_rope", ctypes.c_int32), ("sm_count", ctypes.c_int32),
-        ("total_keys", ctypes.c_int64),
+        ("total_keys", ctypes.c_int64), ("kv_share", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

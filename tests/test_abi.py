@@ -173,3 +173,26 @@ def test_decode_rejects_unknown_variant(lib):
         plan = mla.mla_plan_force_splits(mla.mla_decode_plan(1, 1, 16, 4096, 152), 4)
         plan.variant = variant
         assert _call_decode(lib, plan, ws_bytes=plan.workspace_bytes) == -1, variant
+
+
+def test_kv_share_choice(lib):
+    cases = [((8, 1, 16, 8 * 8192), 1), ((8, 4, 16, 8 * 8192), 2), ((2, 1, 64, 131072), 2),
+             ((64, 1, 128, 1081344), 4), ((1, 3, 40, 1537), 4), ((1, 2, 40, 100), 1),
+             ((3, 7, 5, 10), 2)]
+    for (batch, q_len, heads, keys), share in cases:
+        p = mla.mla_decode_plan(batch, q_len, heads, keys, 152)
+        assert p.kv_share == share, (batch, q_len, heads, p.kv_share)
+        assert p.head_blocks % p.kv_share == 0
+    assert mla.mla_sparse_decode_plan(4, 64, 2048, 152).kv_share == 2
+    assert mla.mla_sparse_decode_plan(4, 128, 2048, 152).kv_share == 4
+    assert mla.mla_sparse_decode_plan(4, 16, 2048, 152).kv_share == 1
+
+
+def test_decode_rejects_inconsistent_kv_share(lib):
+    p16 = mla.mla_decode_plan(1, 1, 16, 4096, 152)    # 16 rows per CTA
+    p64 = mla.mla_decode_plan(1, 1, 64, 4096, 152)    # 2 head blocks of 32
+    for plan, share in [(p16, 2), (p64, 4), (p64, 3), (p64, 0), (p64, 8)]:
+        q = mla.mla_plan_t.from_buffer_copy(plan)
+        q.kv_share = share
+        heads = q.num_heads
+        assert _call_decode(lib, q, ws_bytes=q.workspace_bytes, heads=heads) == -1, share

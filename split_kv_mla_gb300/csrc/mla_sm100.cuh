@@ -256,6 +256,29 @@ __device__ __forceinline__ void tmem_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// One column per lane (32x32b shape, one register).
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r)
+                 : "memory");
+}
+
+// Pin registers written by tcgen05.ld to the point after tcgen05.wait::ld: the
+// compiler may not move their uses above it.
+template <int K>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[K])
+{
+#pragma unroll
+    for (int i = 0; i < K; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 __device__ __forceinline__ void tmem_wait_st()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

@@ -33,10 +33,12 @@
 //   eight); twelve warps keep the register budget of nine (three warps per SM
 //   sub-partition either way).  TMA keeps the bytes off the SM's load/store path,
 //   which the softmax warps' shared loads and shuffles use.
-// * Lazy rescaling.  A block only recomputes the running maxima when some logit
-//   exceeds them by more than kTau; otherwise p = 2^(s - m) stays below 2^kTau.
-//   The decision is one hardware barrier-reduction (bar.red.or) of the four
-//   softmax warps; O in TMEM is rescaled only at those (rare) blocks.
+// * Lazy rescaling.  Each row keeps a reference m that bounds its logits; p is
+//   2^(s - m).  A block only moves the reference of a row whose logits exceed it
+//   by more than kTau (then to the block maximum plus kHeadroom, so the next
+//   move needs a jump of kTau + kHeadroom); otherwise p stays below 2^kTau.  The
+//   decision is one hardware barrier-reduction (bar.red.or) of the four softmax
+//   warps; O in TMEM is rescaled, column by column, only for the rows that moved.
 // * Sums.  Each block's p (exact fp32, for the LSE) and p_hi + p_lo (what the
 //   MMA consumed, for normalising O) are summed over the warp's 32 keys with a
 //   transposing shuffle reduction, so each lane carries one row's running sums.
@@ -65,8 +67,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kGatherWarps = 7;
 constexpr int kMmaWarp = 7;
 constexpr int kSoftmaxWarp0 = 8;
-constexpr float kTau = 2.f;           // lazy-rescale threshold, base-2 logit units
-constexpr float kShift = 6.f;         // p is fed as p * 2^kShift: at most 2^(kTau + kShift) = 256
+constexpr float kTau = 2.75f;        // lazy-rescale threshold, base-2 logit units
+constexpr float kShift = 6.f;         // p is fed as p * 2^kShift: at most 2^(kTau + kShift) < 448
+constexpr float kHeadroom = 1.f;      // a new reference sits this far above the block maximum
+static_assert(kTau + kShift < 8.807f, "p * 2^kShift stays below e4m3's largest finite 448");
 constexpr int kQWarps = kWarps - kMmaWarp;   // warps 7-11 split the query tile
 constexpr uint32_t kQBar = 2;                // their named barrier (id 1 is the softmax one)
 constexpr uint32_t kGatherSleepNs = 128;
@@ -234,21 +238,23 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 template <int N>
 __device__ __forceinline__ void load_cols(uint32_t taddr, float (&s)[N])
 {
-    uint32_t r[32];
     if (N == 16) {
+        uint32_t r[32];
         tmem_ld32(taddr, r);
         tmem_wait_ld();
+        reg_fence(r);
 #pragma unroll
         for (int n = 0; n < N; ++n) s[n] = __uint_as_float(r[n]) + __uint_as_float(r[(n + N) & 31]);
     } else {
-        tmem_ld32(taddr, r);
+        // both 32-column halves in flight before the one wait
+        uint32_t h[32], l[32];
+        tmem_ld32(taddr, h);
+        tmem_ld32(taddr + 32, l);
         tmem_wait_ld();
+        reg_fence(h);
+        reg_fence(l);
 #pragma unroll
-        for (int n = 0; n < N; ++n) s[n] = __uint_as_float(r[n & 31]);
-        tmem_ld32(taddr + 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int n = 0; n < N; ++n) s[n] += __uint_as_float(r[n & 31]);
+        for (int n = 0; n < N; ++n) s[n] = __uint_as_float(h[n & 31]) + __uint_as_float(l[n & 31]);
     }
 }
 
@@ -272,6 +278,51 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     asm volatile("griddepcontrol.launch_dependents;");
     const int rows_in_req = a.q_len * a.num_heads;
 
+    // With CH > 1 the CH head blocks of one (request, split) form a cluster that
+    // shares every gathered block: rank r issues the r-th share of the block's
+    // copies and multicasts them to all CH CTAs, so each KV byte leaves memory
+    // once.  A stage is refilled only when every CTA of the cluster has finished
+    // its P.V on it (kv_empty collects one arrival per CTA); pv_done is the
+    // CTA's own P.V completion.
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.kv_full[i], kGatherWarps);   // one arrival per gather warp
+            mbar_init(&ms.kv_empty[i], CH);
+            mbar_init(&ms.pv_done[i], 1);
+            mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.s_free[i], 4);
+            mbar_init(&ms.p_full[i], 4);
+        }
+        mbar_init(&ms.o_done, 1);
+        ms.abort = 0;
+        fence_mbar_init();
+    }
+
+    // The query rows' loads go out first, ahead of the index loads and the
+    // gathers that would otherwise queue in front of them (warps 7-11).
+    uint4 qv[C::kQRowsPerWarp][C::kVec];
+    if (warp >= kMmaWarp) {
+        const int qw = warp - kMmaWarp;
+#pragma unroll
+        for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
+            const int n = qw + rr * kQWarps;
+            const int idx = hb * N + n;
+            const bool valid = n < N && idx < rows_in_req;
+            int64_t item = 0;
+            if (valid)
+                item = ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads;
+#pragma unroll
+            for (int v = 0; v < C::kVec; ++v) {
+                const int c = (lane + 32 * v) * 8;
+                qv[rr][v] = make_uint4(0u, 0u, 0u, 0u);
+                if (valid && c < kWidth)
+                    qv[rr][v] = c < a.d_v
+                        ? __ldg(reinterpret_cast<const uint4*>(a.q_lat + item * a.d_v + c))
+                        : __ldg(reinterpret_cast<const uint4*>(a.q_pe + item * a.d_rope + (c - a.d_v)));
+            }
+        }
+    }
+
     // ---- the request's key list and this split's range --------------------------------
     int64_t base;
     int L;
@@ -292,38 +343,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const int k1 = min(L, k0 + chunk);
     const int nblk = (k1 - k0 + kBlockN - 1) / kBlockN;
 
-    // ---- barriers and TMEM ----------------------------------------------------------------
-    // With CH > 1 the CH head blocks of one (request, split) form a cluster that
-    // shares every gathered block: rank r issues the r-th share of the block's
-    // copies and multicasts them to all CH CTAs, so each KV byte leaves memory
-    // once.  A stage is refilled only when every CTA of the cluster has finished
-    // its P.V on it (kv_empty collects one arrival per CTA); pv_done is the
-    // CTA's own P.V completion.
-    if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ms.kv_full[i], kGatherWarps);   // one arrival per gather warp
-            mbar_init(&ms.kv_empty[i], CH);
-            mbar_init(&ms.pv_done[i], 1);
-            mbar_init(&ms.s_full[i], 1);
-            mbar_init(&ms.s_free[i], 4);
-            mbar_init(&ms.p_full[i], 4);
-        }
-        mbar_init(&ms.o_done, 1);
-        ms.abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(&ms.tmem_base, C::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    if (CH > 1)
-        cluster_sync();   // peers' barriers are initialised before any multicast lands
-    else
-        __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = ms.tmem_base;
-    const uint32_t smem_base = smem_u32(smem);
     const int rank = CH > 1 ? (int)cluster_ctarank() : 0;
     constexpr uint16_t kClusterMask = (uint16_t)((1u << CH) - 1u);
 
@@ -411,19 +430,42 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     };
     Slots gnext{};
     int32_t rnext = -1;
+    Slots s0{{-1, -1, -1, -1}}, s1{{-1, -1, -1, -1}};
+    int32_t w0 = -1, w1 = -1;
     if (warp < kGatherWarps && nblk > 0) {
-        // start the first two blocks before anything else
         if (lane == 0) {
             tma_prefetch_desc(&tm_lat);
             if (C::kRope) tma_prefetch_desc(&tm_rope);
         }
-        // the index loads of blocks 0-2 are in flight together
-        const Slots s0 = raw_slots(0);
-        const int32_t w0 = raw_row(0);
-        const Slots s1 = nblk > 1 ? raw_slots(1) : Slots{{-1, -1, -1, -1}};
-        const int32_t w1 = nblk > 1 ? raw_row(1) : -1;
-        gnext = nblk > 2 ? raw_slots(2) : Slots{{-1, -1, -1, -1}};
-        rnext = nblk > 2 ? raw_row(2) : -1;
+        // the index loads of blocks 0-2 are in flight together, during the set-up
+        s0 = raw_slots(0);
+        w0 = raw_row(0);
+        if (nblk > 1) {
+            s1 = raw_slots(1);
+            w1 = raw_row(1);
+        }
+        if (nblk > 2) {
+            gnext = raw_slots(2);
+            rnext = raw_row(2);
+        }
+    }
+
+    // ---- barriers and TMEM ----------------------------------------------------------------
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ms.tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    if (CH > 1)
+        cluster_sync();   // peers' barriers are initialised before any multicast lands
+    else
+        __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms.tmem_base;
+    const uint32_t smem_base = smem_u32(smem);
+
+    if (warp < kGatherWarps && nblk > 0) {
+        // start the first two blocks before anything else
         issue(0, fix_slots(s0), row_valid(0, w0));
         if (nblk > 1) issue(1, fix_slots(s1), row_valid(1, w1));
     }
@@ -435,25 +477,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     if (warp >= kMmaWarp) {
         const int qw = warp - kMmaWarp;
         uint8_t* qtile = smem + C::kOffQ;
-        uint4 qv[C::kQRowsPerWarp][C::kVec];
-#pragma unroll
-        for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
-            const int n = qw + rr * kQWarps;
-            const int idx = hb * N + n;
-            const bool valid = n < N && idx < rows_in_req;
-            int64_t item = 0;
-            if (valid)
-                item = ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads;
-#pragma unroll
-            for (int v = 0; v < C::kVec; ++v) {
-                const int c = (lane + 32 * v) * 8;
-                qv[rr][v] = make_uint4(0u, 0u, 0u, 0u);
-                if (valid && c < kWidth)
-                    qv[rr][v] = c < a.d_v
-                        ? __ldg(reinterpret_cast<const uint4*>(a.q_lat + item * a.d_v + c))
-                        : __ldg(reinterpret_cast<const uint4*>(a.q_pe + item * a.d_rope + (c - a.d_v)));
-            }
-        }
 #pragma unroll
         for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
             const int n = qw + rr * kQWarps;
@@ -685,17 +708,19 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = r;
                 softmax_bar();
                 float alpha[N];
-                bool rescale = false;
+                uint32_t moved = 0;   // rows whose maximum moved (same bits in every thread)
 #pragma unroll
                 for (int n = 0; n < N; ++n) {
                     const float bm = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]),
                                            fmaxf(ms.red[2][n], ms.red[3][n]));
-                    const float mn = fmaxf(m_ref[n], bm);
+                    // only a row whose logits passed its reference by more than
+                    // kTau moves it (bm is -inf when the row saw no valid key)
+                    const float mn = bm > m_ref[n] + kTau ? bm + kHeadroom : m_ref[n];
                     float al = 1.f;
-                    if (mn != -CUDART_INF_F)
+                    if (mn != m_ref[n])
                         al = (m_ref[n] == -CUDART_INF_F) ? 0.f : exp2f(m_ref[n] - mn);
                     alpha[n] = al;
-                    rescale |= al != 1.f;
+                    if (al != 1.f) moved |= 1u << n;
                     m_ref[n] = mn;
                 }
                 float a_mine = 1.f;
@@ -704,23 +729,35 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                     if (n == my_row) a_mine = alpha[n];
                 l_acc *= a_mine;
                 lt_acc *= a_mine;
-                if (rescale && blk > 0) {
-                    // O^T holds blocks < blk: wait for the last P.V, then scale its columns.
+                if (moved != 0 && blk > 0) {
+                    // O^T holds blocks < blk: wait for the last P.V, then scale the
+                    // columns (hi and lo, four d_v chunks) of the rows whose
+                    // maximum moved; alpha is the same in every thread, so the
+                    // loop over rows is uniform.
                     if (warp_wait(&ms.pv_done[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag)) {
                         tc_fence_after();
 #pragma unroll 1
-                        for (int c = 0; c < 4; ++c) {
+                        while (moved != 0) {
+                            const int n = __ffs(moved) - 1;
+                            moved &= moved - 1;
+                            float an = 1.f;
 #pragma unroll
-                            for (int h = 0; h < NC / 32; ++h) {
-                                uint32_t rr[32];
-                                const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + h * 32;
-                                tmem_ld32(ta, rr);
-                                tmem_wait_ld();
+                            for (int k = 0; k < N; ++k)
+                                if (k == n) an = alpha[k];
+                            uint32_t r[8];
 #pragma unroll
-                                for (int k = 0; k < 32; ++k)
-                                    rr[k] = __float_as_uint(__uint_as_float(rr[k]) *
-                                                            alpha[(h * 32 + k) % N]);
-                                tmem_st32(ta, rr);
+                            for (int c = 0; c < 4; ++c) {
+                                const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + n;
+                                r[2 * c] = tmem_ld1(ta);
+                                r[2 * c + 1] = tmem_ld1(ta + N);
+                            }
+                            tmem_wait_ld();
+                            reg_fence(r);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + n;
+                                tmem_st1(ta, __float_as_uint(__uint_as_float(r[2 * c]) * an));
+                                tmem_st1(ta + N, __float_as_uint(__uint_as_float(r[2 * c + 1]) * an));
                             }
                         }
                         tmem_wait_st();

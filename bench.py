@@ -59,7 +59,43 @@ def make_workload(name: str):
     if name.startswith("c4-"):
         t = int(name[3:])
         return "sparse", gen.workload_c4(t), f"T={t} H=64 top-k 2048 of 131072, 448+64"
+    if name.startswith("p-"):
+        b, s = (int(x) for x in name[2:].split("-"))
+        return "dense", gen.workload_c1(q_len=4, seq=s, batch=b), f"B={b} H=16 q_len=4 S={s}"
     raise SystemExit(f"unknown workload {name}")
+
+
+# The pages' MI300X results for the same dense shapes (H=16, q_len=4, shuffled
+# page-size-1 slots, KV bytes only): (B, S) -> TB/s ("Results -- MLA decode",
+# moonmath-ai/amd-kernels README).  Context on other hardware, not the target.
+PAGES_MI300X_TBS = {(1, 150000): 1.13, (2, 150000): 1.54, (8, 8192): 0.73, (8, 32768): 1.48,
+                    (8, 65536): 1.67, (8, 150000): 1.75, (16, 150000): 1.70, (32, 8192): 1.45}
+
+
+def pages_baseline_gbs(name: str):
+    """The pages' GB/s for exactly this workload, or None."""
+    if name == "c1q4":
+        key = (8, 8192)
+    elif name.startswith("p-"):
+        key = tuple(int(x) for x in name[2:].split("-"))
+    else:
+        return None
+    v = PAGES_MI300X_TBS.get(key)
+    return None if v is None else v * 1000.0
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks (every rank gets it)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_call: int, world: int, ms_per_call: float) -> float:
+    """Whole-job GB/s: every rank's calls over the slowest rank's time."""
+    return bytes_per_call * world / (ms_per_call * 1e-3) / 1e9
 
 
 def keys_per_call(kind, inp) -> int:
@@ -226,14 +262,6 @@ class Runner:
             fn(plan, d["q_nope"], d["q_pe"], d["pool"], d["indices"], inp.scale, inp.kv_scale,
                o=self.o, lse=self.lse, workspace_t=self.ws, stream=stream)
 
-    def reduce(self, stream):
-        o_part, lse_part = self.mla.mla_workspace_partials(self.plan, self.ws)
-        if o_part is None:
-            return
-        self.mla.mla_splitk_reduce(o_part, lse_part, self.inp.kv_scale,
-                                   o=self.o.view(-1, self.o.shape[-1]),
-                                   lse=self.lse.view(-1), stream=stream)
-
     def launches_per_step(self):
         return 1 if self.plan.num_splits == 1 else 2
 
@@ -261,23 +289,31 @@ def time_steps(runner, stream, steps, copies):
     return g_full, g_rem, full, start, end
 
 
-def kernel_times(runner, stream, n):
-    """Average device duration (ms) of the split kernel and the reduce kernel,
-    from events recorded around each launch on the launching stream."""
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
-    plan = runner.plan
+def kernel_times(runner, stream, steps, step_ms):
+    """Average device duration (ms) of the split kernel, and the rest of a call
+    (the split-K reduce and its launch), from CUDA events on the launching stream
+    around CUDA-graph replays of split-kernel-only calls over the same rotating
+    inputs; the rest is the whole call's time minus the split kernel's."""
+    if runner.plan.num_splits == 1:
+        return step_ms, 0.0
+    copies = len(runner.copies)
+    g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        torch.cuda._sleep(50_000_000)  # let the host enqueue ahead of the device
-        for i in range(n):
-            evs[i][0].record(stream)
-            runner.step(i, stream, splits_only=True, plan=plan)
-            evs[i][1].record(stream)
-            runner.reduce(stream)
-            evs[i][2].record(stream)
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(copies):
+                runner.step(i, stream, splits_only=True)
+    reps = max(1, steps // copies)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
     torch.cuda.synchronize()
-    split = [e[0].elapsed_time(e[1]) for e in evs]
-    red = [e[1].elapsed_time(e[2]) for e in evs]
-    return statistics.mean(split), statistics.mean(red)
+    split_ms = start.elapsed_time(end) / (reps * copies)
+    return split_ms, max(0.0, step_ms - split_ms)
 
 
 def e2e_measure(runner, stream, steps):
@@ -427,16 +463,15 @@ def run_ours(args, rank, world, local_rank):
     sampler.stop()
     clocks = sampler.summary()
 
-    if world > 1:
-        t = torch.tensor([ms_total], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, device)
     ms_step = ms_total / args.steps
     bytes_call = kv_bytes_per_call(kind, inp)
-    value = bytes_call * world / (ms_step * 1e-3) / 1e9
+    value = job_gbs(bytes_call, world, ms_step)
 
-    split_ms, reduce_ms = kernel_times(runner, stream, min(200, max(20, args.steps)))
+    split_ms, reduce_ms = kernel_times(runner, stream, min(2000, max(200, args.steps)), ms_step)
+    split_ms = max_over_ranks(split_ms, world, device)
     e2e_ms, h2d, d2h = e2e_measure(runner, stream, min(200, max(20, args.steps)))
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
     peak, peak_src = measured_peaks()
     achieved = bytes_call / (split_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
@@ -446,7 +481,10 @@ def run_ours(args, rank, world, local_rank):
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3fn-kv/bf16-q/fp32-acc",
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (round(value / pages_baseline_gbs(args.workload), 3)
+                        if pages_baseline_gbs(args.workload) else None),
+        "dtype": "e4m3fn-kv/bf16-q/fp32-acc",
         "data": "synthetic (seeded; N(0,1) bf16 queries, N(0,1)/kv_scale e4m3fn pool, shuffled page_size-1 slots)",
         "config": {"workload": f"{args.workload}: dense MLA decode {desc}" if kind == "dense"
                    else f"{args.workload}: sparse top-k MLA decode {desc}",
@@ -459,14 +497,16 @@ def run_ours(args, rank, world, local_rank):
         "us_per_call": ms_step * 1e3,
         "keys_per_s": keys_per_call(kind, inp) * world / (ms_step * 1e-3),
         "hbm_frac_of_measured": round(value / world / peak, 4),
+        "hbm_frac_of_spec_8tbs": round(value / world / 8000.0, 4),
         "gpu_launches": args.steps * runner.launches_per_step(),
-        "kernels": {"split_ms": split_ms, "reduce_ms": reduce_ms,
-                    "split_share": split_ms / (split_ms + reduce_ms) if reduce_ms > 0 else 1.0},
+        "kernels": {"split_ms": split_ms, "rest_ms": reduce_ms,
+                    "split_share": split_ms / (split_ms + reduce_ms) if reduce_ms > 0 else 1.0,
+                    "timing": "graph replays of split-kernel-only calls; rest = call - split"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peak_src, "kernel": "split kernel",
                      "algorithmic_bytes": bytes_call},
-        "e2e": {"value": round(bytes_call / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_gbs(bytes_call, world, e2e_ms), 2), "unit": "GB/s",
                 "us_per_call": e2e_ms * 1e3, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks,

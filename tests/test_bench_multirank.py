@@ -1,0 +1,73 @@
+"""Host logic of bench.py's multi-rank path (independent replicas under
+torch.distributed), run with world size 2 over gloo on the CPU: every rank gets
+the slowest rank's time, the whole-job value counts every rank's work over that
+time, and the reference arm prints from rank 0 only."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        out[rank] = bench.max_over_ranks(1.5 + 2.0 * rank, world, "cpu")
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_world_size_2_gloo():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        mp.start_processes(_worker, args=(2, _free_port(), out), nprocs=2, join=True,
+                           start_method="spawn")
+        assert dict(out) == {0: 3.5, 1: 3.5}
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(4.25, 1, "cpu") == 4.25
+
+
+def test_job_value_counts_every_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.job_gbs(10**9, 1, 1.0) == pytest.approx(1000.0)
+    assert bench.job_gbs(10**9, 4, 2.0) == pytest.approx(2000.0)
+
+
+def test_reference_arm_runs_on_rank_0_only():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        workload, steps, warmup, ref_requests = "c0", 1, 0, 1
+    assert bench.run_reference(A(), 1, 2) is None
+
+
+def test_pages_baseline_only_for_the_pages_own_shapes():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.pages_baseline_gbs("c1q4") == pytest.approx(730.0)
+    assert bench.pages_baseline_gbs("p-16-150000") == pytest.approx(1700.0)
+    assert bench.pages_baseline_gbs("c1q1") is None
+    assert bench.pages_baseline_gbs("c3") is None

@@ -548,11 +548,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             if (j >= 0) warp_wait(&ms.kv_full[j & 1], (j >> 1) & 1, &drain_abort, kGatherSleepNs);
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer =====================================================
-        // Order per block j: P.V of block j-1 as soon as its P is ready (frees that
-        // stage for the gather of block j+1 as early as possible), then Q.K^T of
-        // block j.  Descriptors are built once per stage and advanced by adding
-        // the byte offset / 16 to their address field (shared memory < 256 KB, so
-        // the 14-bit field never carries).
+        // Descriptors are built once per stage and advanced by adding the byte
+        // offset / 16 to their address field (shared memory < 256 KB, so the
+        // 14-bit field never carries).
         if (lane == 0 && nblk > 0) {
             const uint32_t id_qk = idesc_e4m3(128, NC, false, false);
             const uint32_t id_pv = idesc_e4m3(128, NC, true, true);
@@ -603,34 +601,46 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 }
                 umma_commit(&ms.s_full[st]);
             };
-            bool alive = true;
-            for (int blk = 0; blk < nblk && alive; ++blk) {
-                const int st = blk & 1;
-                if (blk >= 1) {
-                    if (!mbar_wait_or_abort(&ms.p_full[(blk - 1) & 1], ((blk - 1) >> 1) & 1,
-                                            abort_flag, kMmaSleepNs)) {
-                        alive = false;
+            // Event loop: QK of the next block as soon as its rows have landed
+            // and its S buffer is free (so QK of block j+1 runs while the
+            // softmax works on block j), P.V of the oldest block as soon as its
+            // P is published (which frees the block's stage).  Both conditions
+            // are polled without blocking; P.V goes first when both are ready.
+            // No progress for kWaitLimitCycles ends the loop with the abort flag.
+            int next_qk = 0, next_pv = 0;
+            long long t_last = clock64();
+            for (uint32_t idle = 0; next_pv < nblk;) {
+                bool did = false;
+                if (next_pv < next_qk &&
+                    mbar_try_wait(&ms.p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+                    tc_fence_after();
+                    issue_pv(next_pv);
+                    if (next_pv == nblk - 1) umma_commit(&ms.o_done);
+                    ++next_pv;
+                    did = true;
+                }
+                if (next_qk < nblk &&
+                    mbar_try_wait(&ms.kv_full[next_qk & 1], (next_qk >> 1) & 1) &&
+                    (next_qk < 2 ||
+                     mbar_try_wait(&ms.s_free[next_qk & 1], ((next_qk - 2) >> 1) & 1))) {
+                    tc_fence_after();
+                    issue_qk(next_qk);
+                    ++next_qk;
+                    did = true;
+                }
+                if (did) {
+                    idle = 0;
+                    continue;
+                }
+                if (++idle > 4) __nanosleep(kMmaSleepNs);
+                if ((idle & 63u) == 0) {
+                    const long long now = clock64();
+                    if (*abort_flag) break;
+                    if (idle == 64) t_last = now;   // first check of this idle stretch
+                    else if (now - t_last > kWaitLimitCycles) {
+                        *abort_flag = 1;
                         break;
                     }
-                    tc_fence_after();
-                    issue_pv(blk - 1);
-                }
-                if (!mbar_wait_or_abort(&ms.kv_full[st], (blk >> 1) & 1, abort_flag, kMmaSleepNs) ||
-                    (blk >= 2 && !mbar_wait_or_abort(&ms.s_free[st], ((blk - 2) >> 1) & 1,
-                                                     abort_flag, kMmaSleepNs))) {
-                    alive = false;
-                    break;
-                }
-                tc_fence_after();
-                issue_qk(blk);
-            }
-            if (alive && !*abort_flag) {
-                const int last = nblk - 1;
-                if (mbar_wait_or_abort(&ms.p_full[last & 1], (last >> 1) & 1, abort_flag,
-                                       kMmaSleepNs)) {
-                    tc_fence_after();
-                    issue_pv(last);
-                    umma_commit(&ms.o_done);
                 }
             }
         }

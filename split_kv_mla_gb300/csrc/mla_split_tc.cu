@@ -39,9 +39,11 @@
 //   move needs a jump of kTau + kHeadroom); otherwise p stays below 2^kTau.  The
 //   decision is one hardware barrier-reduction (bar.red.or) of the four softmax
 //   warps; O in TMEM is rescaled, column by column, only for the rows that moved.
-// * Sums.  Each block's p (exact fp32, for the LSE) and p_hi + p_lo (what the
-//   MMA consumed, for normalising O) are summed over the warp's 32 keys with a
-//   transposing shuffle reduction, so each lane carries one row's running sums.
+// * Sums.  Each block's exact fp32 p (for the LSE) is summed over the warp's
+//   32 keys with a transposing shuffle reduction, so each lane carries one row's
+//   running sum.  The sums of p_hi + p_lo (what the tensor core consumed, used
+//   to normalise O) come from the tensor core itself: a fifth P.V chunk whose A
+//   operand is an all-ones tile accumulates them next to O.
 // * Safety.  Every mbarrier wait is time-bounded and warp-uniform; the softmax
 //   warps meet at bar.sync only at points every one of them reaches, and agree
 //   on giving up through the same barrier-reduction, so a stuck pipeline ends
@@ -51,6 +53,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <climits>
 #include <mutex>
 
 #include "mla_internal.h"
@@ -90,16 +93,22 @@ struct Cfg {
     static constexpr int kOffStage = 0;
     static constexpr int kOffQ = 2 * kStageBytes;
     static constexpr int kOffP = kOffQ + kQBytes;
-    static constexpr int kOffMisc = kOffP + 2 * kPBytes;
-    static constexpr uint32_t kTmemCols = (6 * NC <= 256) ? 256u : 512u;
+    // An all-ones e4m3 tile (1.0 = 0x38) as the A operand of a fifth P.V chunk:
+    // its output is the column sums of P^T, i.e. the row sums of the p_hi + p_lo
+    // the tensor core consumed (any layout of a constant tile is the same tile).
+    static constexpr int kOffOnes = (kOffP + 2 * kPBytes + 1023) / 1024 * 1024;
+    static constexpr int kOnesBytes = kBlockN * 128;
+    static constexpr int kOffMisc = kOffOnes + kOnesBytes;
+    static constexpr uint32_t kTmemCols = (7 * NC <= 256) ? 256u : 512u;
     static constexpr uint32_t kColS = 0;                   // S^T buffers: [0, 2 NC)
-    static constexpr uint32_t kColO = 2 * NC;              // O^T chunks:  [2 NC, 6 NC)
+    static constexpr uint32_t kColO = 2 * NC;              // O^T chunks:  [2 NC, 6 NC), sums [6 NC, 7 NC)
     static constexpr int kGroups = kRowBytes / 8;          // 8-column query groups per row
     static constexpr int kVec = (kGroups + 31) / 32;       // query groups per lane
     static constexpr int kQRowsPerWarp = (N + kQWarps - 1) / kQWarps;
     static_assert(kOffQ % 1024 == 0 && kQChunkBytes % 1024 == 0, "128B-swizzle atoms");
     static_assert(kOffP % 16 == 0, "P tile alignment");
-    static_assert(6 * NC <= 512, "TMEM columns");
+    static_assert(7 * NC <= 512, "TMEM columns");
+    static_assert(kOffOnes % 1024 == 0, "ones tile alignment");
     static_assert(N * 512 * 4 <= 2 * kStageBytes, "epilogue staging fits in the stages");
 };
 
@@ -109,10 +118,9 @@ struct Misc {
     int abort;
     int kvalid[2][kBlockN];
     alignas(16) float cq[32];   // per query row: raw dot -> base-2 logit
-    int win[32];        // per query row: keys at positions < win are visible
+    alignas(16) int win[32];   // per query row: keys at positions < win are visible
     float red[4][32];   // cross-warp reduction scratch
-    float red2[4][32];  // second reduction scratch (epilogue: the lt sums)
-    alignas(16) float fin[2][32];   // epilogue: 1 / lt and the base-2 LSE per row
+    alignas(16) float fin[2][32];   // epilogue: the base-2 LSE per row (fin[1])
     long long row_item[32];   // epilogue: output row (request row x head) per query row, -1 if none
 };
 
@@ -451,6 +459,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
 
     // ---- barriers and TMEM ----------------------------------------------------------------
+    {
+        uint4* ones = reinterpret_cast<uint4*>(smem + C::kOffOnes);
+        for (int i = tid; i < C::kOnesBytes / 16; i += kThreads)
+            ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+        fence_proxy_async_smem();
+    }
     if (warp == kMmaWarp) {
         tmem_alloc(&ms.tmem_base, C::kTmemCols);
         tmem_relinquish();
@@ -562,6 +576,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             const uint64_t qk_b_rope = smem_desc(qb + 4 * C::kQChunkBytes, 16, 512, kSw64);
             const uint64_t pv_a = smem_desc(stage0, C::kLatChunkBytes, 1024, kSw128);
             const uint64_t pv_b = smem_desc(smem_base + C::kOffP, 128, 2048, kSwNone);
+            const uint64_t pv_ones = smem_desc(smem_base + C::kOffOnes, C::kLatChunkBytes, 1024, kSw128);
             auto issue_pv = [&](int blk) {
                 const int st = blk & 1;
                 const uint64_t a0 = pv_a + (uint64_t)((st * C::kStageBytes) >> 4);
@@ -574,6 +589,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                 a0 + (uint64_t)((c * C::kLatChunkBytes + kk * 4096) >> 4),
                                 b0 + (uint64_t)((kk * 512) >> 4), id_pv,
                                 (blk > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_f8(tmem + C::kColO + 4 * NC, pv_ones + (uint64_t)((kk * 4096) >> 4),
+                            b0 + (uint64_t)((kk * 512) >> 4), id_pv,
+                            (blk > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&ms.pv_done[st]);
                 // the stage may be refilled once every CTA of the cluster is done
                 // with it (the last two blocks' stages are never refilled)
@@ -656,7 +676,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         float m_ref[N];
 #pragma unroll
         for (int n = 0; n < N; ++n) m_ref[n] = -CUDART_INF_F;
-        float l_acc = 0.f, lt_acc = 0.f;          // running sums of row my_row over this warp's keys
+        float l_acc = 0.f;                        // running sum of row my_row over this warp's keys
         bool alive = true;
         for (int blk = 0; blk < nblk; ++blk) {
             const int st = blk & 1;
@@ -690,17 +710,18 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 cq[4 * g + 2] = v.z;
                 cq[4 * g + 3] = v.w;
             }
+            // Visible window per row: everything but keys past the request's
+            // end for the row's draft position (only tail blocks can clip).
+            const int jt = tail ? j : INT_MIN;
             bool need = false;
-            if (!tail) {
 #pragma unroll
-                for (int n = 0; n < N; ++n) {
-                    s[n] = kval ? s[n] * cq[n] : -CUDART_INF_F;
-                    need |= s[n] > m_ref[n] + kTau;
-                }
-            } else {
+            for (int g = 0; g < N / 4; ++g) {
+                const int4 w = reinterpret_cast<const int4*>(ms.win)[g];
+                const int wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int n = 0; n < N; ++n) {
-                    const bool vis = kval && j < ms.win[n];
+                for (int u = 0; u < 4; ++u) {
+                    const int n = 4 * g + u;
+                    const bool vis = kval && jt < wv[u];
                     s[n] = vis ? s[n] * cq[n] : -CUDART_INF_F;
                     need |= s[n] > m_ref[n] + kTau;
                 }
@@ -738,7 +759,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 for (int n = 0; n < N; ++n)
                     if (n == my_row) a_mine = alpha[n];
                 l_acc *= a_mine;
-                lt_acc *= a_mine;
                 if (moved != 0 && blk > 0) {
                     // O^T holds blocks < blk: wait for the last P.V, then scale the
                     // columns (hi and lo, four d_v chunks) of the rows whose
@@ -754,9 +774,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
                             for (int k = 0; k < N; ++k)
                                 if (k == n) an = alpha[k];
-                            uint32_t r[8];
+                            uint32_t r[10];
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
+                            for (int c = 0; c < 5; ++c) {
                                 const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + n;
                                 r[2 * c] = tmem_ld1(ta);
                                 r[2 * c + 1] = tmem_ld1(ta + N);
@@ -764,7 +784,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                             tmem_wait_ld();
                             reg_fence(r);
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
+                            for (int c = 0; c < 5; ++c) {
                                 const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + n;
                                 tmem_st1(ta, __float_as_uint(__uint_as_float(r[2 * c]) * an));
                                 tmem_st1(ta + N, __float_as_uint(__uint_as_float(r[2 * c + 1]) * an));
@@ -776,7 +796,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
             // P^T row ti: bytes [0, N) = p_hi, [N, 2N) = p_lo, of p * 2^kShift.
             if (blk >= 2) warp_wait(&ms.pv_done[st], ((blk - 2) >> 1) & 1, abort_flag);
-            float pt[N];
             uint32_t hiw[N / 4], low[N / 4];
 #pragma unroll
             for (int n = 0; n < N; n += 4) {
@@ -787,12 +806,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                    ? 0.f : exp2f(x - m_ref[n + u] + kShift);
                 }
                 uint16_t h0, l0, h1, l1;
-                const float2 v0 = split_pair(s[n], s[n + 1], h0, l0);
-                const float2 v1 = split_pair(s[n + 2], s[n + 3], h1, l1);
-                pt[n] = v0.x;
-                pt[n + 1] = v0.y;
-                pt[n + 2] = v1.x;
-                pt[n + 3] = v1.y;
+                split_pair(s[n], s[n + 1], h0, l0);
+                split_pair(s[n + 2], s[n + 3], h1, l1);
                 hiw[n / 4] = (uint32_t)h0 | ((uint32_t)h1 << 16);
                 low[n / 4] = (uint32_t)l0 | ((uint32_t)l1 << 16);
             }
@@ -812,30 +827,25 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             // The empty asm keeps the compiler from scheduling these shuffles
             // ahead of the P hand-off above, where they would delay the MMA.
 #pragma unroll
-            for (int n = 0; n < N; ++n) asm volatile("" : "+f"(s[n]), "+f"(pt[n]));
+            for (int n = 0; n < N; ++n) asm volatile("" : "+f"(s[n]));
             l_acc += warp_transpose_reduce<N, false>(s, lane);
-            lt_acc += warp_transpose_reduce<N, false>(pt, lane);
         }
 
         // ---- epilogue ------------------------------------------------------------------------
-        // Row sums over all 128 keys -> 1/lt and the base-2 LSE per row, and each
-        // row's output index; then O^T leaves TMEM already normalised (times
-        // 1/lt, and kv_scale into bf16 for a single split) into the idle KV
-        // stages, and one bulk TMA store per row writes it out.
-        if ((lane % kLanesPerRow) == 0) {
-            ms.red[sw][my_row] = l_acc;
-            ms.red2[sw][my_row] = lt_acc;
-        }
+        // Row sums over all 128 keys -> the base-2 LSE per row (from the exact
+        // fp32 p), and each row's output index; the sums of what the MMA
+        // consumed (lt) sit in the fifth O chunk.  O^T leaves TMEM already
+        // normalised (times 1/lt, and kv_scale into bf16 for a single split)
+        // into the idle KV stages, and one bulk TMA store per row writes it out.
+        if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = l_acc;
         softmax_bar();
         const int ns = a.num_splits;
         if (ti < N) {
             const float lsum = ms.red[0][ti] + ms.red[1][ti] + ms.red[2][ti] + ms.red[3][ti];
-            const float ltsum = ms.red2[0][ti] + ms.red2[1][ti] + ms.red2[2][ti] + ms.red2[3][ti];
             float mr = 0.f;
 #pragma unroll
             for (int n = 0; n < N; ++n)
                 if (n == ti) mr = m_ref[n];
-            ms.fin[0][ti] = ltsum > 0.f ? 1.f / ltsum : 0.f;
             ms.fin[1][ti] = lsum > 0.f ? mr + log2f(lsum) - kShift : -CUDART_INF_F;
             const int idx = hb * N + ti;
             ms.row_item[ti] = idx < rows_in_req
@@ -846,13 +856,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (have_o) tc_fence_after();
         softmax_bar();
         float inv[N];
+        if (have_o) {
+            load_cols<N>(tmem + lane_addr + C::kColO + 4 * NC, inv);
 #pragma unroll
-        for (int g = 0; g < N / 4; ++g) {
-            const float4 v = reinterpret_cast<const float4*>(ms.fin[0])[g];
-            inv[4 * g] = v.x;
-            inv[4 * g + 1] = v.y;
-            inv[4 * g + 2] = v.z;
-            inv[4 * g + 3] = v.w;
+            for (int n = 0; n < N; ++n) inv[n] = inv[n] > 0.f ? __frcp_rn(inv[n]) : 0.f;
+        } else {
+#pragma unroll
+            for (int n = 0; n < N; ++n) inv[n] = 0.f;
         }
         const bool final_rows = ns == 1;
         float* ostage = reinterpret_cast<float*>(smem + C::kOffStage);              // fp32 [N][512]

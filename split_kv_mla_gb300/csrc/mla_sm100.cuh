@@ -159,6 +159,23 @@ __device__ __forceinline__ void tma_gather4_multicast(void* dst, const void* tma
         : "memory");
 }
 
+// ---- register reallocation between warpgroups ---------------------------------------------
+
+// Lower / raise this warpgroup's registers per thread (all four warps of the
+// warpgroup execute it).  Raising waits until lowered warpgroups have released
+// enough of the block's registers.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_lower()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_raise()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ---- thread-block clusters ---------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -223,6 +240,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
         : "r"(taddr));
 }
 

@@ -21,18 +21,20 @@
 //   precise as rounding p to bf16).  hi and lo are stacked along N (2N MMA
 //   columns), so the big operand is read from shared memory once per MMA.
 //   kv_scale and the powers of two are folded into the logit and output scales.
-// * Warp roles.  Warps 0-6 gather the block's 128 rows with TMA tile::gather4
-//   (four slots per instruction; 128-byte latent boxes land 128B-swizzled, the
-//   64-byte RoPE box 64B-swizzled: exactly the K-major operand layout) into a
-//   two-stage ring, the block's 160 copies dealt out over the seven warps; warp 7
-//   issues the tcgen05.mma (kind::f8f6f4, fp32 accumulators in TMEM) and commits
-//   to mbarriers; warps 8-11 own one TMEM lane (= one key) each and run the online
-//   base-2 softmax.  Measured on GB300, a warp issues one gather4 about every 100
-//   cycles, so a block's issue time falls with the number of issuing warps (per
-//   SM, random 576-byte rows gather at ~38 GB/s from four warps, ~54 GB/s from
-//   eight); twelve warps keep the register budget of nine (three warps per SM
-//   sub-partition either way).  TMA keeps the bytes off the SM's load/store path,
-//   which the softmax warps' shared loads and shuffles use.
+// * Warp roles (16 warps).  Warps 0-6 gather the block's 128 rows with TMA
+//   tile::gather4 (four slots per instruction; 128-byte latent boxes land
+//   128B-swizzled, the 64-byte RoPE box 64B-swizzled: exactly the K-major operand
+//   layout) into a two-stage ring, the block's 160 copies dealt out over the
+//   seven warps; warp 7 issues the tcgen05.mma (kind::f8f6f4, fp32 accumulators
+//   in TMEM) and commits to mbarriers; warps 8-11 and 12-15 are two softmax sets,
+//   each owning half the query rows, and warp w % 4 of a set owns TMEM lanes
+//   32 (w % 4)..+31 (one key per thread).  Measured on GB300, a warp issues one
+//   gather4 about every 100 cycles, so a block's issue time falls with the number
+//   of issuing warps (per SM, random 576-byte rows gather at ~38 GB/s from four
+//   warps, ~54 GB/s from eight); and one softmax warp per SM sub-partition left
+//   its dependent chains exposed, so every key has two.  Registers move with
+//   setmaxnreg from warpgroups 0-1 (64 per thread) to the softmax warpgroups
+//   (192).
 // * Lazy rescaling.  Each row keeps a reference m that bounds its logits; p is
 //   2^(s - m).  A block only moves the reference of a row whose logits exceed it
 //   by more than kTau (then to the block maximum plus kHeadroom, so the next
@@ -65,17 +67,21 @@ namespace {
 using namespace sm100;
 
 constexpr int kBlockN = 128;          // keys per block (MMA M)
-constexpr int kThreads = 384;         // warps 0-6 gather, warp 7 MMA, warps 8-11 softmax
+constexpr int kThreads = 512;         // warps 0-6 gather, 7 MMA, 8-11 and 12-15 softmax
 constexpr int kWarps = kThreads / 32;
 constexpr int kGatherWarps = 7;
 constexpr int kMmaWarp = 7;
-constexpr int kSoftmaxWarp0 = 8;
+constexpr int kSoftmaxWarp0 = 8;      // two sets of four warps, each set owns half the rows
+constexpr int kSets = 2;
+constexpr uint32_t kRegsLow = 64;     // registers per thread of warpgroups 0-1 after set-up
+constexpr uint32_t kRegsHigh = 192;   // ... of the softmax warpgroups 2-3
+static_assert(2 * 128 * kRegsLow + 2 * 128 * kRegsHigh == 65536, "register split = the file");
 constexpr float kTau = 2.75f;        // lazy-rescale threshold, base-2 logit units
 constexpr float kShift = 6.f;         // p is fed as p * 2^kShift: at most 2^(kTau + kShift) < 448
 constexpr float kHeadroom = 1.f;      // a new reference sits this far above the block maximum
 static_assert(kTau + kShift < 8.807f, "p * 2^kShift stays below e4m3's largest finite 448");
-constexpr int kQWarps = kWarps - kMmaWarp;   // warps 7-11 split the query tile
-constexpr uint32_t kQBar = 2;                // their named barrier (id 1 is the softmax one)
+constexpr int kQWarps = kWarps - kSoftmaxWarp0;   // warps 8-15 split the query tile
+constexpr uint32_t kQBar = 2;                     // Q tile + MMA warp (1 and 3: softmax sets)
 constexpr uint32_t kGatherSleepNs = 128;
 constexpr uint32_t kMmaSleepNs = 32;
 
@@ -119,7 +125,7 @@ struct Misc {
     int kvalid[2][kBlockN];
     alignas(16) float cq[32];   // per query row: raw dot -> base-2 logit
     alignas(16) int win[32];   // per query row: keys at positions < win are visible
-    float red[4][32];   // cross-warp reduction scratch
+    float red[8][32];   // cross-warp reduction scratch, [set * 4 + warp of the set][row]
     alignas(16) float fin[2][32];   // epilogue: the base-2 LSE per row (fin[1])
     long long row_item[32];   // epilogue: output row (request row x head) per query row, -1 if none
 };
@@ -211,24 +217,24 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane)
     return v[0];
 }
 
-// Barrier of the four softmax warps (id 1, 128 threads).  Only used at points
-// that all four warps always reach.
-__device__ __forceinline__ void softmax_bar()
+// Barrier of the four warps of one softmax set (id 1 or 3, 128 threads).  Only
+// used at points that all four warps of the set always reach.
+__device__ __forceinline__ void softmax_bar(uint32_t id)
 {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
 
-// The same barrier, returning the OR of `v` over the four warps.
-__device__ __forceinline__ bool softmax_bar_or(bool v)
+// The same barrier, returning the OR of `v` over the set's four warps.
+__device__ __forceinline__ bool softmax_bar_or(uint32_t id, bool v)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, 1, 128, pi;\n\t"
+        "setp.ne.u32 pi, %2, 0;\n\t"
+        "bar.red.or.pred po, %1, 128, pi;\n\t"
         "selp.u32 %0, 1, 0, po;\n\t}"
         : "=r"(r)
-        : "r"(v ? 1u : 0u)
+        : "r"(id), "r"(v ? 1u : 0u)
         : "memory");
     return r != 0;
 }
@@ -242,27 +248,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
-// One TMEM row of N query-row columns: hi column n plus lo column N + n.
-template <int N>
-__device__ __forceinline__ void load_cols(uint32_t taddr, float (&s)[N])
+// One TMEM row of R query-row columns: hi columns at taddr_hi plus lo columns
+// at taddr_lo (the two halves of the stacked MMA output), summed.
+template <int R>
+__device__ __forceinline__ void load_rows(uint32_t taddr_hi, uint32_t taddr_lo, float (&s)[R])
 {
-    if (N == 16) {
-        uint32_t r[32];
-        tmem_ld32(taddr, r);
-        tmem_wait_ld();
-        reg_fence(r);
-#pragma unroll
-        for (int n = 0; n < N; ++n) s[n] = __uint_as_float(r[n]) + __uint_as_float(r[(n + N) & 31]);
-    } else {
-        // both 32-column halves in flight before the one wait
-        uint32_t h[32], l[32];
-        tmem_ld32(taddr, h);
-        tmem_ld32(taddr + 32, l);
+    static_assert(R == 8 || R == 16, "a softmax set holds 8 or 16 rows");
+    if constexpr (R == 16) {
+        uint32_t h[16], l[16];
+        tmem_ld16(taddr_hi, h);
+        tmem_ld16(taddr_lo, l);
         tmem_wait_ld();
         reg_fence(h);
         reg_fence(l);
 #pragma unroll
-        for (int n = 0; n < N; ++n) s[n] = __uint_as_float(h[n & 31]) + __uint_as_float(l[n & 31]);
+        for (int n = 0; n < R; ++n) s[n] = __uint_as_float(h[n]) + __uint_as_float(l[n]);
+    } else {
+        uint32_t h[8], l[8];
+        tmem_ld8(taddr_hi, h);
+        tmem_ld8(taddr_lo, l);
+        tmem_wait_ld();
+        reg_fence(h);
+        reg_fence(l);
+#pragma unroll
+        for (int n = 0; n < R; ++n) s[n] = __uint_as_float(h[n]) + __uint_as_float(l[n]);
     }
 }
 
@@ -298,8 +307,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             mbar_init(&ms.kv_empty[i], CH);
             mbar_init(&ms.pv_done[i], 1);
             mbar_init(&ms.s_full[i], 1);
-            mbar_init(&ms.s_free[i], 4);
-            mbar_init(&ms.p_full[i], 4);
+            mbar_init(&ms.s_free[i], 4 * kSets);   // every softmax warp
+            mbar_init(&ms.p_full[i], 4 * kSets);
         }
         mbar_init(&ms.o_done, 1);
         ms.abort = 0;
@@ -307,10 +316,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
 
     // The query rows' loads go out first, ahead of the index loads and the
-    // gathers that would otherwise queue in front of them (warps 7-11).
+    // gathers that would otherwise queue in front of them (warps 8-15).
     uint4 qv[C::kQRowsPerWarp][C::kVec];
-    if (warp >= kMmaWarp) {
-        const int qw = warp - kMmaWarp;
+    if (warp >= kSoftmaxWarp0) {
+        const int qw = warp - kSoftmaxWarp0;
 #pragma unroll
         for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
             const int n = qw + rr * kQWarps;
@@ -484,12 +493,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (nblk > 1) issue(1, fix_slots(s1), row_valid(1, w1));
     }
 
-    // ---- the query tile: one warp per row, warps 7-11 --------------------------------------------
+    // ---- the query tile: one warp per row, warps 8-15 --------------------------------------------
     // q is scaled by 2^sh so that max |q| is in [128, 256), then split into e4m3
     // hi (tile rows 0..N-1) and lo (rows N..2N-1).  The gather warps go on
     // loading meanwhile; the MMA warp waits for the tile at the warps' barrier.
-    if (warp >= kMmaWarp) {
-        const int qw = warp - kMmaWarp;
+    if (warp >= kSoftmaxWarp0) {
+        const int qw = warp - kSoftmaxWarp0;
         uint8_t* qtile = smem + C::kOffQ;
 #pragma unroll
         for (int rr = 0; rr < C::kQRowsPerWarp; ++rr) {
@@ -535,11 +544,16 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
         }
     }
-    if (warp >= kMmaWarp) {
+    if (warp >= kMmaWarp) {   // the query warps and the MMA warp, which waits for the tile
         fence_proxy_async_smem();
-        asm volatile("bar.sync %0, %1;" ::"n"(kQBar), "n"(kQWarps * 32) : "memory");
+        asm volatile("bar.sync %0, %1;" ::"n"(kQBar), "n"((kQWarps + 1) * 32) : "memory");
     }
 
+    // Registers move from the gather and MMA warpgroups (0-1) to the softmax
+    // warpgroups (2-3); the shares add up to the block's 512 x 128 registers.
+    // Each branch below holds all of its warpgroups' remaining code.
+    if (warp < kSoftmaxWarp0) {
+    regs_lower<kRegsLow>();
     if (warp < kGatherWarps) {
         // ================= gather ============================================================
         // block j reuses the stage of block j-2: wait for its P.V, then load
@@ -665,85 +679,86 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
         }
         __syncwarp();
+    }
     } else {
-        // ================= softmax + epilogue (warps 8..11) ====================================
-        const int sw = warp - kSoftmaxWarp0;      // 0..3
-        const int quad = warp & 3;                // TMEM lane quadrant of this warp
-        const int ti = quad * 32 + lane;          // key within a block == TMEM lane
+        regs_raise<kRegsHigh>();
+        // ================= softmax + epilogue (warps 8..15) ====================================
+        // Two sets of four warps; set s owns query rows [s R, s R + R) (R = N / 2)
+        // and warp w % 4 of a set owns TMEM lanes 32 (w % 4) .. +31 (one key per
+        // thread), so two warps work on every key.
+        constexpr int R = N / kSets;
+        const int set = (warp - kSoftmaxWarp0) / 4;       // 0 or 1
+        const int sw = (warp - kSoftmaxWarp0) % 4;        // warp within the set
+        const uint32_t bar_id = 1u + 2u * (uint32_t)set;  // the set's named barrier
+        const int r0 = set * R;                           // the set's first row
+        const int quad = warp & 3;                        // TMEM lane quadrant of this warp
+        const int ti = quad * 32 + lane;                  // key within a block == TMEM lane
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-        constexpr int kLanesPerRow = 32 / N;      // lanes holding the same row after a reduction
-        const int my_row = lane / kLanesPerRow;   // the row whose sums this lane carries
-        float m_ref[N];
+        constexpr int kLanesPerRow = 32 / R;              // lanes holding one row after a reduction
+        const int my_row = lane / kLanesPerRow;           // set row whose sum this lane carries
+        float* red = &ms.red[set * 4][0];                 // [4][32] of this set
+        float m_ref[R];
 #pragma unroll
-        for (int n = 0; n < N; ++n) m_ref[n] = -CUDART_INF_F;
-        float l_acc = 0.f;                        // running sum of row my_row over this warp's keys
+        for (int n = 0; n < R; ++n) m_ref[n] = -CUDART_INF_F;
+        float l_acc = 0.f;                                // running sum of row r0 + my_row over the warp's keys
         bool alive = true;
         for (int blk = 0; blk < nblk; ++blk) {
             const int st = blk & 1;
             const uint32_t ph = (blk >> 1) & 1;
             bool ok = warp_wait(&ms.kv_full[st], ph, abort_flag) &&
                       warp_wait(&ms.s_full[st], ph, abort_flag);
-            float s[N];
+            float s[R];
             if (ok) {
                 tc_fence_after();
-                load_cols<N>(tmem + lane_addr + C::kColS + st * NC, s);
+                const uint32_t sa = tmem + lane_addr + C::kColS + st * NC + r0;
+                load_rows<R>(sa, sa + N, s);
             } else {
 #pragma unroll
-                for (int n = 0; n < N; ++n) s[n] = -CUDART_INF_F;
+                for (int n = 0; n < R; ++n) s[n] = -CUDART_INF_F;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.s_free[st]);
             const bool kval = ms.kvalid[st][ti] != 0;
             const int j = k0 + blk * kBlockN + ti;
-            // Per-row logit scales as 16-byte loads issued together, and a
+            // Per-row logit scales and windows as 16-byte loads, and a
             // branch-free mask.  The draft window only bites in blocks that reach
-            // the last q_len - 1 positions of the request (kval already drops keys
-            // beyond the split); elsewhere every row sees every valid key.
+            // the last q_len - 1 positions of the request (kval already drops
+            // keys beyond the split).
             const bool tail = k0 + (blk + 1) * kBlockN > L - a.q_len + 1;
-            float cq[N];
-#pragma unroll
-            for (int g = 0; g < N / 4; ++g) {
-                const float4 v = reinterpret_cast<const float4*>(ms.cq)[g];
-                cq[4 * g] = v.x;
-                cq[4 * g + 1] = v.y;
-                cq[4 * g + 2] = v.z;
-                cq[4 * g + 3] = v.w;
-            }
-            // Visible window per row: everything but keys past the request's
-            // end for the row's draft position (only tail blocks can clip).
             const int jt = tail ? j : INT_MIN;
             bool need = false;
 #pragma unroll
-            for (int g = 0; g < N / 4; ++g) {
-                const int4 w = reinterpret_cast<const int4*>(ms.win)[g];
-                const int wv[4] = {w.x, w.y, w.z, w.w};
+            for (int g = 0; g < R / 4; ++g) {
+                const float4 c4 = reinterpret_cast<const float4*>(ms.cq + r0)[g];
+                const int4 w4 = reinterpret_cast<const int4*>(ms.win + r0)[g];
+                const float cq[4] = {c4.x, c4.y, c4.z, c4.w};
+                const int wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int n = 4 * g + u;
                     const bool vis = kval && jt < wv[u];
-                    s[n] = vis ? s[n] * cq[n] : -CUDART_INF_F;
+                    s[n] = vis ? s[n] * cq[u] : -CUDART_INF_F;
                     need |= s[n] > m_ref[n] + kTau;
                 }
             }
-            if (softmax_bar_or(!ok || *abort_flag)) {
+            if (softmax_bar_or(bar_id, !ok || *abort_flag)) {
                 alive = false;
                 break;
             }
-            if (softmax_bar_or(need)) {
-                // new running maxima: block max over the 128 keys, all four warps
-                float v[N];
+            if (softmax_bar_or(bar_id, need)) {
+                // new references: block max over the 128 keys, the set's four warps
+                float v[R];
 #pragma unroll
-                for (int n = 0; n < N; ++n) v[n] = s[n];
-                const float r = warp_transpose_reduce<N, true>(v, lane);
-                if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = r;
-                softmax_bar();
-                float alpha[N];
-                uint32_t moved = 0;   // rows whose maximum moved (same bits in every thread)
+                for (int n = 0; n < R; ++n) v[n] = s[n];
+                const float r = warp_transpose_reduce<R, true>(v, lane);
+                if ((lane % kLanesPerRow) == 0) red[sw * 32 + my_row] = r;
+                softmax_bar(bar_id);
+                float alpha[R];
+                uint32_t moved = 0;   // rows whose reference moved (same bits in every thread)
 #pragma unroll
-                for (int n = 0; n < N; ++n) {
-                    const float bm = fmaxf(fmaxf(ms.red[0][n], ms.red[1][n]),
-                                           fmaxf(ms.red[2][n], ms.red[3][n]));
+                for (int n = 0; n < R; ++n) {
+                    const float bm = fmaxf(fmaxf(red[n], red[32 + n]), fmaxf(red[64 + n], red[96 + n]));
                     // only a row whose logits passed its reference by more than
                     // kTau moves it (bm is -inf when the row saw no valid key)
                     const float mn = bm > m_ref[n] + kTau ? bm + kHeadroom : m_ref[n];
@@ -756,14 +771,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 }
                 float a_mine = 1.f;
 #pragma unroll
-                for (int n = 0; n < N; ++n)
+                for (int n = 0; n < R; ++n)
                     if (n == my_row) a_mine = alpha[n];
                 l_acc *= a_mine;
                 if (moved != 0 && blk > 0) {
                     // O^T holds blocks < blk: wait for the last P.V, then scale the
-                    // columns (hi and lo, four d_v chunks) of the rows whose
-                    // maximum moved; alpha is the same in every thread, so the
-                    // loop over rows is uniform.
+                    // columns (hi and lo, four d_v chunks and the sums) of the rows
+                    // whose reference moved; the loop over rows is uniform.
                     if (warp_wait(&ms.pv_done[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag)) {
                         tc_fence_after();
 #pragma unroll 1
@@ -772,33 +786,34 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                             moved &= moved - 1;
                             float an = 1.f;
 #pragma unroll
-                            for (int k = 0; k < N; ++k)
+                            for (int k = 0; k < R; ++k)
                                 if (k == n) an = alpha[k];
-                            uint32_t r[10];
+                            uint32_t rr[10];
 #pragma unroll
                             for (int c = 0; c < 5; ++c) {
-                                const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + n;
-                                r[2 * c] = tmem_ld1(ta);
-                                r[2 * c + 1] = tmem_ld1(ta + N);
+                                const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + r0 + n;
+                                rr[2 * c] = tmem_ld1(ta);
+                                rr[2 * c + 1] = tmem_ld1(ta + N);
                             }
                             tmem_wait_ld();
-                            reg_fence(r);
+                            reg_fence(rr);
 #pragma unroll
                             for (int c = 0; c < 5; ++c) {
-                                const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + n;
-                                tmem_st1(ta, __float_as_uint(__uint_as_float(r[2 * c]) * an));
-                                tmem_st1(ta + N, __float_as_uint(__uint_as_float(r[2 * c + 1]) * an));
+                                const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + r0 + n;
+                                tmem_st1(ta, __float_as_uint(__uint_as_float(rr[2 * c]) * an));
+                                tmem_st1(ta + N, __float_as_uint(__uint_as_float(rr[2 * c + 1]) * an));
                             }
                         }
                         tmem_wait_st();
                     }
                 }
             }
-            // P^T row ti: bytes [0, N) = p_hi, [N, 2N) = p_lo, of p * 2^kShift.
+            // P^T row ti: bytes [0, N) = p_hi, [N, 2N) = p_lo, of p * 2^kShift; this
+            // set writes bytes [r0, r0 + R) of each half.
             if (blk >= 2) warp_wait(&ms.pv_done[st], ((blk - 2) >> 1) & 1, abort_flag);
-            uint32_t hiw[N / 4], low[N / 4];
+            uint32_t hiw[R / 4], low[R / 4];
 #pragma unroll
-            for (int n = 0; n < N; n += 4) {
+            for (int n = 0; n < R; n += 4) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const float x = s[n + u];
@@ -811,24 +826,27 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 hiw[n / 4] = (uint32_t)h0 | ((uint32_t)h1 << 16);
                 low[n / 4] = (uint32_t)l0 | ((uint32_t)l1 << 16);
             }
+            // P^T is stored as 16-column blocks of 128 keys x 16 bytes
             uint8_t* prow = smem + C::kOffP + st * C::kPBytes + ti * 16;
-#pragma unroll
-            for (int g = 0; g < N / 16; ++g) {
-                *reinterpret_cast<uint4*>(prow + g * 2048) =
-                    make_uint4(hiw[4 * g], hiw[4 * g + 1], hiw[4 * g + 2], hiw[4 * g + 3]);
-                *reinterpret_cast<uint4*>(prow + (N / 16 + g) * 2048) =
-                    make_uint4(low[4 * g], low[4 * g + 1], low[4 * g + 2], low[4 * g + 3]);
+            if constexpr (R == 16) {
+                *reinterpret_cast<uint4*>(prow + set * 2048) =
+                    make_uint4(hiw[0], hiw[1], hiw[2], hiw[3]);
+                *reinterpret_cast<uint4*>(prow + (N / 16 + set) * 2048) =
+                    make_uint4(low[0], low[1], low[2], low[3]);
+            } else {
+                *reinterpret_cast<uint2*>(prow + set * 8) = make_uint2(hiw[0], hiw[1]);
+                *reinterpret_cast<uint2*>(prow + (N / 16) * 2048 + set * 8) = make_uint2(low[0], low[1]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.p_full[st]);
-            // Running sums of this warp's 32 keys (lane ends up with row my_row).
-            // The empty asm keeps the compiler from scheduling these shuffles
-            // ahead of the P hand-off above, where they would delay the MMA.
+            // Running sums of this warp's 32 keys (lane ends up with set row
+            // my_row).  The empty asm keeps the compiler from scheduling these
+            // shuffles ahead of the P hand-off above, where they would delay the MMA.
 #pragma unroll
-            for (int n = 0; n < N; ++n) asm volatile("" : "+f"(s[n]));
-            l_acc += warp_transpose_reduce<N, false>(s, lane);
+            for (int n = 0; n < R; ++n) asm volatile("" : "+f"(s[n]));
+            l_acc += warp_transpose_reduce<R, false>(s, lane);
         }
 
         // ---- epilogue ------------------------------------------------------------------------
@@ -837,66 +855,71 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         // consumed (lt) sit in the fifth O chunk.  O^T leaves TMEM already
         // normalised (times 1/lt, and kv_scale into bf16 for a single split)
         // into the idle KV stages, and one bulk TMA store per row writes it out.
-        if ((lane % kLanesPerRow) == 0) ms.red[sw][my_row] = l_acc;
-        softmax_bar();
+        // Each set handles its own rows.
+        if ((lane % kLanesPerRow) == 0) red[sw * 32 + my_row] = l_acc;
+        softmax_bar(bar_id);
         const int ns = a.num_splits;
-        if (ti < N) {
-            const float lsum = ms.red[0][ti] + ms.red[1][ti] + ms.red[2][ti] + ms.red[3][ti];
+        if (ti < R) {
+            const int row = r0 + ti;
+            const float lsum = red[ti] + red[32 + ti] + red[64 + ti] + red[96 + ti];
             float mr = 0.f;
 #pragma unroll
-            for (int n = 0; n < N; ++n)
+            for (int n = 0; n < R; ++n)
                 if (n == ti) mr = m_ref[n];
-            ms.fin[1][ti] = lsum > 0.f ? mr + log2f(lsum) - kShift : -CUDART_INF_F;
-            const int idx = hb * N + ti;
-            ms.row_item[ti] = idx < rows_in_req
+            ms.fin[1][row] = lsum > 0.f ? mr + log2f(lsum) - kShift : -CUDART_INF_F;
+            const int idx = hb * N + row;
+            ms.row_item[row] = idx < rows_in_req
                 ? ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads
                 : -1;
         }
         const bool have_o = alive && nblk > 0 && warp_wait(&ms.o_done, 0, abort_flag);
         if (have_o) tc_fence_after();
-        softmax_bar();
-        float inv[N];
+        softmax_bar(bar_id);
+        float inv[R];
         if (have_o) {
-            load_cols<N>(tmem + lane_addr + C::kColO + 4 * NC, inv);
+            const uint32_t la = tmem + lane_addr + C::kColO + 4 * NC + r0;
+            load_rows<R>(la, la + N, inv);
 #pragma unroll
-            for (int n = 0; n < N; ++n) inv[n] = inv[n] > 0.f ? __frcp_rn(inv[n]) : 0.f;
+            for (int n = 0; n < R; ++n) inv[n] = inv[n] > 0.f ? __frcp_rn(inv[n]) : 0.f;
         } else {
 #pragma unroll
-            for (int n = 0; n < N; ++n) inv[n] = 0.f;
+            for (int n = 0; n < R; ++n) inv[n] = 0.f;
         }
         const bool final_rows = ns == 1;
         float* ostage = reinterpret_cast<float*>(smem + C::kOffStage);              // fp32 [N][512]
         uint16_t* ostage16 = reinterpret_cast<uint16_t*>(smem + C::kOffStage);      // bf16 [N][512]
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-            float o[N];
+            float o[R];
             if (have_o) {
-                load_cols<N>(tmem + lane_addr + C::kColO + c * NC, o);
+                const uint32_t oa = tmem + lane_addr + C::kColO + c * NC + r0;
+                load_rows<R>(oa, oa + N, o);
             } else {
 #pragma unroll
-                for (int n = 0; n < N; ++n) o[n] = 0.f;
+                for (int n = 0; n < R; ++n) o[n] = 0.f;
             }
             if (final_rows) {
 #pragma unroll
-                for (int n = 0; n < N; ++n)
-                    ostage16[n * 512 + c * 128 + ti] =
+                for (int n = 0; n < R; ++n)
+                    ostage16[(r0 + n) * 512 + c * 128 + ti] =
                         __bfloat16_as_ushort(__float2bfloat16_rn(o[n] * (inv[n] * a.out_scale)));
             } else {
 #pragma unroll
-                for (int n = 0; n < N; ++n) ostage[n * 512 + c * 128 + ti] = o[n] * inv[n];
+                for (int n = 0; n < R; ++n) ostage[(r0 + n) * 512 + c * 128 + ti] = o[n] * inv[n];
             }
         }
         fence_proxy_async_smem();
-        softmax_bar();
-        if (ti < N) {
-            const long long item = ms.row_item[ti];
+        softmax_bar(bar_id);
+        if (ti < R) {
+            const int row = r0 + ti;
+            const long long item = ms.row_item[row];
             if (item >= 0) {
                 if (final_rows) {
-                    bulk_store(a.o + item * C::kDv, ostage16 + ti * 512, C::kDv * 2);
-                    if (a.lse) a.lse[item] = ms.fin[1][ti];
+                    bulk_store(a.o + item * C::kDv, ostage16 + row * 512, C::kDv * 2);
+                    if (a.lse) a.lse[item] = ms.fin[1][row];
                 } else {
-                    bulk_store(a.o_part + (item * ns + split) * C::kDv, ostage + ti * 512, C::kDv * 4);
-                    a.lse_part[item * ns + split] = ms.fin[1][ti];
+                    bulk_store(a.o_part + (item * ns + split) * C::kDv, ostage + row * 512, C::kDv * 4);
+                    a.lse_part[item * ns + split] = ms.fin[1][row];
                 }
                 bulk_commit();
                 bulk_wait_read();

@@ -371,6 +371,46 @@ __device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t ct
         : "memory");
 }
 
+// The same three operations for a converged warp: every lane passes the same
+// (warp-uniform) operands and lane 0 alone issues the instruction, predicated
+// rather than branched to, so the operands can stay in uniform registers.  The
+// issuing lane is always lane 0, so commits track that lane's MMAs.
+__device__ __forceinline__ void umma_f8_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .u32 l;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_warp(uint64_t* bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_multicast_warp(uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}"
+        ::"r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
+}
+
 // ---- fp8 helpers -----------------------------------------------------------------------------
 
 // Two fp32 -> packed e4m3x2 (round to nearest even, saturating to +-448);

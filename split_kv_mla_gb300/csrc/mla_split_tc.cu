@@ -576,10 +576,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             if (j >= 0) warp_wait(&ms.kv_full[j & 1], (j >> 1) & 1, &drain_abort, kGatherSleepNs);
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer =====================================================
-        // Descriptors are built once per stage and advanced by adding the byte
-        // offset / 16 to their address field (shared memory < 256 KB, so the
-        // 14-bit field never carries).
-        if (lane == 0 && nblk > 0) {
+        // The whole warp runs this code converged and lane 0 issues each MMA and
+        // commit (predicated, not branched to), so the descriptors stay in
+        // uniform registers; a lone-lane branch cost ~80 cycles per MMA in
+        // register moves.  Descriptors are built once per stage and advanced by
+        // adding the byte offset / 16 to their address field (shared memory <
+        // 256 KB, so the 14-bit field never carries).
+        if (nblk > 0) {
             const uint32_t id_qk = idesc_e4m3(128, NC, false, false);
             const uint32_t id_pv = idesc_e4m3(128, NC, true, true);
             const uint32_t stage0 = smem_base + C::kOffStage;
@@ -599,22 +602,22 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_f8(tmem + C::kColO + c * NC,
+                        umma_f8_warp(tmem + C::kColO + c * NC,
                                 a0 + (uint64_t)((c * C::kLatChunkBytes + kk * 4096) >> 4),
                                 b0 + (uint64_t)((kk * 512) >> 4), id_pv,
                                 (blk > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_f8(tmem + C::kColO + 4 * NC, pv_ones + (uint64_t)((kk * 4096) >> 4),
+                    umma_f8_warp(tmem + C::kColO + 4 * NC, pv_ones + (uint64_t)((kk * 4096) >> 4),
                             b0 + (uint64_t)((kk * 512) >> 4), id_pv,
                             (blk > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&ms.pv_done[st]);
+                umma_commit_warp(&ms.pv_done[st]);
                 // the stage may be refilled once every CTA of the cluster is done
                 // with it (the last two blocks' stages are never refilled)
                 if (CH == 1)
-                    umma_commit(&ms.kv_empty[st]);
+                    umma_commit_warp(&ms.kv_empty[st]);
                 else if (blk + 2 < nblk)
-                    umma_commit_multicast(&ms.kv_empty[st], kClusterMask);
+                    umma_commit_multicast_warp(&ms.kv_empty[st], kClusterMask);
             };
             auto issue_qk = [&](int blk) {
                 const int st = blk & 1;
@@ -624,16 +627,16 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_f8(d, qk_a_lat + soff + (uint64_t)((c * C::kLatChunkBytes + kk * 32) >> 4),
+                        umma_f8_warp(d, qk_a_lat + soff + (uint64_t)((c * C::kLatChunkBytes + kk * 32) >> 4),
                                 qk_b_lat + (uint64_t)((c * C::kQChunkBytes + kk * 32) >> 4), id_qk,
                                 (c > 0 || kk > 0) ? 1u : 0u);
                 if (C::kRope) {
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk)
-                        umma_f8(d, qk_a_rope + soff + (uint64_t)((kk * 32) >> 4),
+                        umma_f8_warp(d, qk_a_rope + soff + (uint64_t)((kk * 32) >> 4),
                                 qk_b_rope + (uint64_t)((kk * 32) >> 4), id_qk, 1u);
                 }
-                umma_commit(&ms.s_full[st]);
+                umma_commit_warp(&ms.s_full[st]);
             };
             // Event loop: QK of the next block as soon as its rows have landed
             // and its S buffer is free (so QK of block j+1 runs while the
@@ -643,20 +646,21 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             // No progress for kWaitLimitCycles ends the loop with the abort flag.
             int next_qk = 0, next_pv = 0;
             long long t_last = clock64();
+            // a poll's outcome comes from lane 0, so every lane takes the same path
+            auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
+                return __shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1 : 0, 0) != 0;
+            };
             for (uint32_t idle = 0; next_pv < nblk;) {
                 bool did = false;
-                if (next_pv < next_qk &&
-                    mbar_try_wait(&ms.p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+                if (next_pv < next_qk && ready(&ms.p_full[next_pv & 1], (next_pv >> 1) & 1)) {
                     tc_fence_after();
                     issue_pv(next_pv);
-                    if (next_pv == nblk - 1) umma_commit(&ms.o_done);
+                    if (next_pv == nblk - 1) umma_commit_warp(&ms.o_done);
                     ++next_pv;
                     did = true;
                 }
-                if (next_qk < nblk &&
-                    mbar_try_wait(&ms.kv_full[next_qk & 1], (next_qk >> 1) & 1) &&
-                    (next_qk < 2 ||
-                     mbar_try_wait(&ms.s_free[next_qk & 1], ((next_qk - 2) >> 1) & 1))) {
+                if (next_qk < nblk && ready(&ms.kv_full[next_qk & 1], (next_qk >> 1) & 1) &&
+                    (next_qk < 2 || ready(&ms.s_free[next_qk & 1], ((next_qk - 2) >> 1) & 1))) {
                     tc_fence_after();
                     issue_qk(next_qk);
                     ++next_qk;

@@ -12,7 +12,8 @@
 // CTAs can be scheduled while the split kernel drains, and griddepcontrol.wait
 // holds them until the split kernel has completed and its writes are visible.
 // Launched after anything else (or without the launch attribute) the wait
-// returns at once.
+// returns at once.  It lets its own dependents (the next split kernel, whose
+// set-up then overlaps this kernel) be scheduled once every row has started.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -34,6 +35,8 @@ splitk_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__
     __shared__ float fscale;
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next call's split kernel may be scheduled as soon as all rows started
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t row = blockIdx.x;
     if (row >= rows) return;
     const int tid = threadIdx.x;

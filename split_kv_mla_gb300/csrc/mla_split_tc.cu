@@ -314,6 +314,21 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         ms.abort = 0;
         fence_mbar_init();
     }
+    {
+        uint4* ones = reinterpret_cast<uint4*>(smem + C::kOffOnes);
+        for (int i = tid; i < C::kOnesBytes / 16; i += kThreads)
+            ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+        fence_proxy_async_smem();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ms.tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    // Everything above touches only this CTA's shared memory and TMEM.  This
+    // launch is a programmatic dependent of the preceding kernel, which may
+    // still be writing the inputs (queries, page table, cache rows): wait for it
+    // before the first global read.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // The query rows' loads go out first, ahead of the index loads and the
     // gathers that would otherwise queue in front of them (warps 8-15).
@@ -468,16 +483,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
 
     // ---- barriers and TMEM ----------------------------------------------------------------
-    {
-        uint4* ones = reinterpret_cast<uint4*>(smem + C::kOffOnes);
-        for (int i = tid; i < C::kOnesBytes / 16; i += kThreads)
-            ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
-        fence_proxy_async_smem();
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(&ms.tmem_base, C::kTmemCols);
-        tmem_relinquish();
-    }
     tc_fence_before();
     if (CH > 1)
         cluster_sync();   // peers' barriers are initialised before any multicast lands
@@ -995,15 +1000,19 @@ cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, cons
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute la[1];
+    cudaLaunchAttribute la[2];
+    // a programmatic dependent of the preceding kernel: set-up overlaps its tail
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
     if (CH > 1) {
         // the CH head blocks of one (request, split) share every gathered block
-        la[0].id = cudaLaunchAttributeClusterDimension;
-        la[0].val.clusterDim.x = CH;
-        la[0].val.clusterDim.y = 1;
-        la[0].val.clusterDim.z = 1;
-        cfg.attrs = la;
-        cfg.numAttrs = 1;
+        la[1].id = cudaLaunchAttributeClusterDimension;
+        la[1].val.clusterDim.x = CH;
+        la[1].val.clusterDim.y = 1;
+        la[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, split_tc_kernel<N, SPARSE, CH>, lat, rope, a);
 }

@@ -82,7 +82,7 @@ constexpr float kHeadroom = 1.f;      // a new reference sits this far above the
 static_assert(kTau + kShift < 8.807f, "p * 2^kShift stays below e4m3's largest finite 448");
 constexpr int kQWarps = kWarps - kSoftmaxWarp0;   // warps 8-15 split the query tile
 constexpr uint32_t kQBar = 2;                     // Q tile + MMA warp (1 and 3: softmax sets)
-constexpr uint32_t kGatherSleepNs = 128;
+constexpr uint32_t kGatherSleepNs = 32;
 constexpr uint32_t kMmaSleepNs = 32;
 
 template <int N, bool SPARSE>

@@ -267,6 +267,21 @@ int mla_decode_noalloc(const mla_plan_t* plan, const void* q_lat, const void* q_
 const char* mla_status_string(int status);
 
 /*
+ * Gather probe, for tests of the page-table gather (step a2): copies
+ * out[i, :] = pool[indices[i], :] for i < n, byte for byte, through the split
+ * kernel's own gather path (TMA tile::gather4 into the swizzled shared-memory
+ * stage layout, then read back de-swizzled).  row_bytes is 576 (dense rows:
+ * four 128-byte chunks and a 64-byte RoPE chunk) or 512 (sparse rows).  An
+ * index outside [0, pool_rows) is not read; its output row is zero.  pool and
+ * out 16-byte aligned; workspace (>= MLA_WORKSPACE_HEADER_BYTES, 256-byte
+ * aligned) receives MLA_DEVERR_TIMEOUT if a bounded wait ran out.  Not on the
+ * decode path.
+ */
+int mla_debug_gather(const void* pool, int64_t pool_rows, int32_t row_bytes,
+                     const int32_t* indices, int64_t n, void* out, void* workspace,
+                     void* stream);
+
+/*
  * The split count that the wave-fill rule of hip_mha_decoding_num_partitions
  * (MLA-style branch) gives for the given constants: ctas = ceil(heads/bm) *
  * batch; one_wave = sm/ctas; two_wave = 2*sm/ctas; pages = ceil(keys/page);

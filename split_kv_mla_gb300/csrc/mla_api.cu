@@ -477,6 +477,24 @@ int mla_read_device_error(const void* workspace, int32_t* code, void* stream)
     return MLA_OK;
 }
 
+int mla_debug_gather(const void* pool, int64_t pool_rows, int32_t row_bytes,
+                     const int32_t* indices, int64_t n, void* out, void* workspace, void* stream)
+{
+    if (n < 0 || pool_rows < 1 || (row_bytes != 576 && row_bytes != 512))
+        return row_bytes != 576 && row_bytes != 512 ? MLA_ERR_UNSUPPORTED_SHAPE : MLA_ERR_INVALID_ARG;
+    if (n == 0) return MLA_OK;
+    if (!pool || !indices || !out || !workspace) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(pool) || !aligned16(out)) return MLA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLA_ERR_MISALIGNED;
+    int rc = device_ok();
+    if (rc != MLA_OK) return rc;
+    cudaError_t e = launch_gather_probe(pool, pool_rows, row_bytes, indices, n,
+                                        static_cast<uint8_t*>(out),
+                                        static_cast<uint32_t*>(workspace),
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH_FAILED;
+}
+
 const char* mla_status_string(int status)
 {
     switch (status) {

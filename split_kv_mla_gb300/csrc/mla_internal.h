@@ -1,6 +1,7 @@
 // mla_internal.h -- host-side declarations shared by the libmla translation units.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/mla_decode.h"
@@ -39,6 +40,16 @@ enum Variant : int32_t {
 };
 
 cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream);
+
+// 2-D uint8 tensor map of the pool (row_bytes columns x rows) with one-row
+// boxes of `box` columns (the shape tile::gather4 reads); false on failure.
+bool make_row_map(CUtensorMap* m, const void* pool, int64_t rows, int row_bytes, int box,
+                  CUtensorMapSwizzle sw);
+
+// Gather probe (mla_debug_gather).
+cudaError_t launch_gather_probe(const void* pool, int64_t pool_rows, int32_t row_bytes,
+                                const int32_t* indices, int64_t n, uint8_t* out, uint32_t* err,
+                                cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
                                  int32_t num_splits, int32_t d_v, float out_scale,
                                  uint16_t* o, float* lse, cudaStream_t stream);

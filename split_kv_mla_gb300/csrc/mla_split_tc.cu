@@ -59,6 +59,7 @@
 #include <mutex>
 
 #include "mla_internal.h"
+#include "mla_layout.cuh"
 #include "mla_sm100.cuh"
 
 namespace mla {
@@ -136,22 +137,6 @@ constexpr int smem_bytes()
     return Cfg<N, SPARSE>::kOffMisc + (int)sizeof(Misc);
 }
 
-
-// Byte offset of column c (0 <= c < row width) of operand row `row` in a tile
-// of `rows` rows laid out as four 128B-swizzled 128-column chunks followed by
-// one 64B-swizzled 64-column chunk (the canonical K-major layouts; the same
-// bytes read as MN-major give V^T).
-__device__ __forceinline__ int tile_offset(int row, int c, int rows)
-{
-    if (c < 512) {
-        const int chunk = c >> 7, kb = c & 127;
-        return chunk * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
-               (((kb >> 4) ^ (row & 7)) << 4) + (kb & 15);
-    }
-    const int kb = c - 512;
-    return 4 * rows * 128 + (row >> 3) * 512 + (row & 7) * 64 +
-           (((kb >> 4) ^ ((row & 7) >> 1)) << 4) + (kb & 15);
-}
 
 // x * 2^k, exact whenever the result is a normal fp32 number.
 __device__ __forceinline__ float mul_pow2(float x, int k)
@@ -953,36 +938,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
 // ---- host side -------------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
-// 2-D uint8 map of the pool (row_bytes columns x rows) with one-row boxes of
-// `box` columns: the shape tile::gather4 reads.
-bool make_row_map(CUtensorMap* m, const void* pool, int64_t rows, int row_bytes, int box,
-                  CUtensorMapSwizzle sw)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-    cuuint64_t gstr[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t bdim[2] = {(cuuint32_t)box, 1};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), gdim, gstr, bdim, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int N, bool SPARSE, int CH>
 cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
                            const mla_plan_t& plan, cudaStream_t stream)
@@ -1029,6 +984,36 @@ cudaError_t launch_rows32(const CUtensorMap& lat, const CUtensorMap& rope, const
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// 2-D uint8 map of the pool (row_bytes columns x rows) with one-row boxes of
+// `box` columns: the shape tile::gather4 reads.
+bool make_row_map(CUtensorMap* m, const void* pool, int64_t rows, int row_bytes, int box,
+                  CUtensorMapSwizzle sw)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t gstr[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t bdim[2] = {(cuuint32_t)box, 1};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), gdim, gstr, bdim, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream)
 {

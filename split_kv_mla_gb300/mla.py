@@ -93,6 +93,7 @@ def load(build_if_missing: bool = True):
             "mla_read_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32), vp]),
             "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "mla_wave_fill_splits": (i32, [i32, i64, i32, i32, i32, i32, i32, i32, i32]),
+            "mla_debug_gather": (ctypes.c_int, [vp, i64, i32, vp, i64, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -289,6 +290,25 @@ def mla_read_device_error(workspace_t, stream=None) -> int:
     _check(load().mla_read_device_error(_dev_ptr(workspace_t, "workspace"), ctypes.byref(code),
                                         _stream_ptr(stream)), "mla_read_device_error")
     return int(code.value)
+
+
+def mla_debug_gather(pool, indices, workspace_t=None, stream=None):
+    """Rows pool[indices] copied through the split kernel's gather path (TMA
+    gather4 into the swizzled stage layout, read back de-swizzled); an
+    out-of-range index gives a zero row.  pool: uint8 [N, 576] or [N, 512]
+    (a [N, 1, 576] cache is accepted); indices: int32 [n].  Returns
+    (rows uint8 [n, row_bytes], workspace)."""
+    p = pool.reshape(pool.shape[0], -1)
+    row_bytes = p.shape[1]
+    n = indices.numel()
+    out = torch.empty(n, row_bytes, dtype=torch.uint8, device=p.device)
+    ws = workspace_t if workspace_t is not None else torch.zeros(
+        MLA_WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=p.device)
+    _check(load().mla_debug_gather(_dev_ptr(p, "pool", torch.uint8), p.shape[0], row_bytes,
+                                   _dev_ptr(indices, "indices", torch.int32), n,
+                                   _dev_ptr(out, "out"), _dev_ptr(ws, "workspace"),
+                                   _stream_ptr(stream)), "mla_debug_gather")
+    return out, ws
 
 
 def mla_decode_noalloc(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv_indptr,

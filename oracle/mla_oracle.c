@@ -32,6 +32,15 @@
  *     M = max_s lse2_s;  w_s = 2^(lse2_s - M);
  *     o = out_scale * sum_s w_s o_s / sum_s w_s;  lse2 = M + log2 sum_s w_s.
  *
+ *   Decode context parallelism (README, "MLA absorbed decode" and "Use / MLA
+ *   decode", DCP): rank cp_rank of cp_world holds the positions p of every
+ *   request with p % cp_world == cp_rank, in increasing order, so its local key
+ *   i is the global position i * cp_world + cp_rank; seq_lens counts the rank's
+ *   keys and glen gives the global lengths.  Draft row t of request b sees the
+ *   global positions p <= glen[b] - q_len + t.  The rank returns o and the
+ *   base-2 LSE of its share; the ranks' results combine by the split-K merge
+ *   above with out_scale 1, the ranks playing the part of the splits.
+ *
  *   Sparse variant ("[Perf] pa_decode_sparse ..." issue, "Measurements"): the
  *   same per-row definition with 448 NoPE + 64 RoPE columns, the key list being
  *   the token's row of the top-k index table; a negative index is an invalid
@@ -268,6 +277,55 @@ int oracle_dense_decode(int32_t batch, int32_t q_len, int32_t num_heads,
                                pool, pool_rows, kv_indices + kv_indptr[b], n,
                                scale, kv_scale, o + i * d_v, lse2 + i);
         }
+        if (local != ORACLE_OK) {
+#pragma omp critical
+            rc = local;
+        }
+    }
+    return rc;
+}
+
+/*
+ * One DCP rank's dense decode (same layouts as oracle_dense_decode; glen
+ * [batch] global lengths).  Row t of request b attends its local keys
+ * j < seq_lens[b] whose global position j*cp_world + cp_rank is at most
+ * glen[b] - q_len + t; positions grow with j, so these are a prefix.
+ */
+int oracle_dcp_decode(int32_t batch, int32_t q_len, int32_t num_heads,
+                      int32_t d_v, int32_t d_rope,
+                      const uint16_t* q_lat, const uint16_t* q_pe,
+                      const uint8_t* pool, int64_t pool_rows,
+                      const int32_t* seq_lens, const int32_t* kv_indices,
+                      const int32_t* kv_indptr, const int32_t* glen,
+                      int32_t cp_rank, int32_t cp_world, double scale, double kv_scale,
+                      double* o, double* lse2)
+{
+    if (batch < 0 || q_len <= 0 || num_heads <= 0 || d_v <= 0 || d_rope < 0 ||
+        cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world)
+        return ORACLE_BAD_ARG;
+    if (!q_lat || (d_rope > 0 && !q_pe) || !pool || !seq_lens || !kv_indices ||
+        !kv_indptr || !glen || !o || !lse2)
+        return ORACLE_BAD_ARG;
+    for (int32_t b = 0; b < batch; ++b)
+        if (seq_lens[b] < 0 || seq_lens[b] > kv_indptr[b + 1] - kv_indptr[b])
+            return ORACLE_BAD_ARG;
+    e4m3_table_init();
+    const int64_t items = (int64_t)batch * q_len * num_heads;
+    int rc = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < items; ++i) {
+        int64_t r = i / num_heads;
+        int64_t h = i % num_heads;
+        int64_t b = r / q_len;
+        int64_t t = r % q_len;
+        int64_t last = (int64_t)glen[b] - q_len + t;   /* last visible global position */
+        int64_t n = 0;
+        while (n < seq_lens[b] && n * cp_world + cp_rank <= last)
+            ++n;
+        int local = attend_row(q_lat + (r * num_heads + h) * d_v,
+                               q_pe + (r * num_heads + h) * d_rope, d_v, d_rope,
+                               pool, pool_rows, kv_indices + kv_indptr[b], n,
+                               scale, kv_scale, o + i * d_v, lse2 + i);
         if (local != ORACLE_OK) {
 #pragma omp critical
             rc = local;

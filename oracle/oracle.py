@@ -20,6 +20,7 @@ Two independent implementations live here:
 from __future__ import annotations
 
 import ctypes
+import dataclasses
 import math
 import os
 import subprocess
@@ -79,6 +80,10 @@ def _load():
                                              c_p, c_i64, c_p, c_dbl, c_dbl, c_p, c_i64,
                                              c_p, c_p]
         lib.oracle_sparse_decode.restype = ctypes.c_int
+        lib.oracle_dcp_decode.argtypes = [c_i32, c_i32, c_i32, c_i32, c_i32, c_p, c_p,
+                                          c_p, c_i64, c_p, c_p, c_p, c_p, c_i32, c_i32,
+                                          c_dbl, c_dbl, c_p, c_p]
+        lib.oracle_dcp_decode.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -204,6 +209,69 @@ def sparse_decode(inp, sel: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np
     return o, lse
 
 
+def dcp_shard(inp, cp_rank: int, cp_world: int):
+    """Rank ``cp_rank``'s view of a ``DenseInputs`` under decode context
+    parallelism (moonmath-ai/amd-kernels README, "Use / MLA decode": a rank holds
+    the positions p with p % cp_world == cp_rank).  Returns a ``DenseInputs`` of
+    the same queries whose request b lists only those positions' slots, in
+    increasing position order, and the global lengths ``glen`` (int32 [B])."""
+    lens = inp.seq_lens.tolist()
+    indptr = inp.kv_indptr.tolist()
+    idx = inp.kv_indices.tolist()
+    local_lens, local_idx, local_ptr = [], [], [0]
+    for b in range(inp.batch):
+        mine = [idx[indptr[b] + p] for p in range(lens[b]) if p % cp_world == cp_rank]
+        local_lens.append(len(mine))
+        local_idx.extend(mine)
+        local_ptr.append(len(local_idx))
+    i32 = torch.int32
+    shard = dataclasses.replace(inp, seq_lens=torch.tensor(local_lens, dtype=i32),
+                                kv_indices=torch.tensor(local_idx, dtype=i32),
+                                kv_indptr=torch.tensor(local_ptr, dtype=i32))
+    return shard, torch.tensor(lens, dtype=i32)
+
+
+def dcp_decode(inp, glen: torch.Tensor, cp_rank: int,
+               cp_world: int) -> Tuple[np.ndarray, np.ndarray]:
+    """fp64 decode of one DCP rank's share: ``inp`` holds the rank's keys (local
+    key j = global position j*cp_world + cp_rank), ``glen`` the global lengths.
+    Returns o [B*q_len, H, d_v] and lse2 [B*q_len, H] of the share."""
+    lib = _load()
+    ql, qp = _u16(inp.q_lat), _u16(inp.q_pe)
+    pl = _u8(inp.pool)
+    R, H = inp.batch * inp.q_len, inp.num_heads
+    o = np.zeros((R * H, inp.d_v), dtype=np.float64)
+    lse = np.zeros(R * H, dtype=np.float64)
+    lens = inp.seq_lens.to(torch.int32).contiguous()
+    idx = inp.kv_indices.to(torch.int32).contiguous()
+    if idx.numel() == 0:
+        idx = torch.zeros(1, dtype=torch.int32)
+    ptr = inp.kv_indptr.to(torch.int32).contiguous()
+    gl = glen.to(torch.int32).contiguous()
+    _check(lib.oracle_dcp_decode(
+        inp.batch, inp.q_len, H, inp.d_v, inp.d_rope, _ptr(ql), _ptr(qp), _ptr(pl),
+        pl.shape[0], _ptr(lens), _ptr(idx), _ptr(ptr), _ptr(gl), int(cp_rank),
+        int(cp_world), inp.scale, inp.kv_scale, _ptr(o), _ptr(lse)))
+    return o.reshape(R, H, inp.d_v), lse.reshape(R, H)
+
+
+def dcp_merge_ranks(o_parts: np.ndarray, lse2_parts: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Merge of the ranks' shares: o_parts [W, ...rows, d_v], lse2_parts
+    [W, ...rows] -> o [...rows, d_v], lse2 [...rows], row by row with ``merge``
+    (out_scale 1; the ranks take the place of the splits)."""
+    op = np.asarray(o_parts, dtype=np.float64)
+    lp = np.asarray(lse2_parts, dtype=np.float64)
+    W, d_v = op.shape[0], op.shape[-1]
+    rows_shape = lp.shape[1:]
+    op2 = op.reshape(W, -1, d_v)
+    lp2 = lp.reshape(W, -1)
+    o = np.zeros((op2.shape[1], d_v))
+    lse = np.zeros(op2.shape[1])
+    for r in range(op2.shape[1]):
+        o[r], lse[r] = merge(op2[:, r, :], lp2[:, r])
+    return o.reshape(rows_shape + (d_v,)), lse.reshape(rows_shape)
+
+
 def split_partials(q_lat, q_pe, pool, slots, scale, kv_scale,
                    num_splits: int) -> Tuple[np.ndarray, np.ndarray]:
     """Partials of one row over ``num_splits`` contiguous key ranges of equal
@@ -265,6 +333,33 @@ def brute_force_dense(inp) -> Tuple[np.ndarray, np.ndarray]:
             for h in range(H):
                 q = ql[r][h] + qp[r][h]
                 ov, lv = brute_force_row(q, rows, inp.d_v, inp.scale, inp.kv_scale)
+                o[r, h] = ov
+                lse[r, h] = lv
+    return o, lse
+
+
+def brute_force_dcp(inp, cp_rank: int, cp_world: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Pure-Python decode of one DCP rank's share of a tiny unsharded
+    ``DenseInputs``: row t of request b attends, in increasing order, the global
+    positions p < S_b with p % cp_world == cp_rank and p <= S_b - q_len + t."""
+    dec = _torch_decode_rows(inp.pool)
+    ql = inp.q_lat.to(torch.float64).tolist()
+    qp = inp.q_pe.to(torch.float64).tolist()
+    R, H = inp.batch * inp.q_len, inp.num_heads
+    o = np.zeros((R, H, inp.d_v))
+    lse = np.zeros((R, H))
+    indptr = inp.kv_indptr.tolist()
+    idx = inp.kv_indices.tolist()
+    lens = inp.seq_lens.tolist()
+    for b in range(inp.batch):
+        for t in range(inp.q_len):
+            r = b * inp.q_len + t
+            pos = [p for p in range(lens[b])
+                   if p % cp_world == cp_rank and p <= lens[b] - inp.q_len + t]
+            rows = [dec[idx[indptr[b] + p]] for p in pos]
+            for h in range(H):
+                ov, lv = brute_force_row(ql[r][h] + qp[r][h], rows, inp.d_v,
+                                         inp.scale, inp.kv_scale)
                 o[r, h] = ov
                 lse[r, h] = lv
     return o, lse

@@ -34,6 +34,12 @@ MUTANTS = {
     "merge_natural_base": ("double w = exp2(lse2_parts[s] - m);",
                            "double w = exp(lse2_parts[s] - m);"),
     "merge_lse_drop_sum": ("*lse2 = m + log2(wsum);", "*lse2 = m;"),
+    "dcp_local_positions": ("while (n < seq_lens[b] && n * cp_world + cp_rank <= last)",
+                            "while (n < seq_lens[b] && n <= last)"),
+    "dcp_rank_offset_dropped": ("while (n < seq_lens[b] && n * cp_world + cp_rank <= last)",
+                                "while (n < seq_lens[b] && n * cp_world <= last)"),
+    "dcp_window_exclusive": ("int64_t last = (int64_t)glen[b] - q_len + t;",
+                             "int64_t last = (int64_t)glen[b] - q_len + t - 1;"),
     "sparse_invalid_kept": ("if (slot < 0)\n            continue;\n        if ((int64_t)slot >= pool_rows)",
                             "if (slot < 0)\n            slot = 0;\n        if ((int64_t)slot >= pool_rows)"),
 }

@@ -13,7 +13,11 @@
 * draft window: row t of a q_len=4 call equals a q_len=1 call on the request
   truncated to S - 4 + t + 1 keys (README, "Use / MLA decode");
 * sparse variant: with a full index row it is the dense definition at
-  448 + 64 columns; negative (invalid) entries are skipped.
+  448 + 64 columns; negative (invalid) entries are skipped;
+* decode context parallelism (README, "Use / MLA decode", DCP): the ranks'
+  shares merged equal the unsharded decode (softmax over a union of disjoint
+  key sets), one rank is the plain decode, and each share equals a pure-Python
+  enumeration of the rank's visible global positions.
 """
 import math
 
@@ -307,3 +311,54 @@ def test_nan_byte_is_rejected():
     inp.pool[int(inp.kv_indices[1]), 0, 3] = 0x7F
     with pytest.raises(oracle.OracleError):
         oracle.dense_decode(inp)
+
+
+# ---- decode context parallelism -----------------------------------------------------
+
+@pytest.mark.parametrize("q_len,world,lens", [
+    (1, 2, [9, 1, 0, 6]),
+    (4, 3, [11, 2, 7, 3]),
+    (3, 4, [13, 5, 1, 8]),
+])
+def test_dcp_shares_merge_to_the_unsharded_decode(q_len, world, lens):
+    inp = gen.dense_inputs(len(lens), q_len, 2, lens, seed=61 + world, extra_slots=4)
+    o_ref, lse_ref = oracle.dense_decode(inp)
+    parts, lses = [], []
+    for k in range(world):
+        shard, glen = oracle.dcp_shard(inp, k, world)
+        o_k, l_k = oracle.dcp_decode(shard, glen, k, world)
+        parts.append(o_k)
+        lses.append(l_k)
+    o, lse = oracle.dcp_merge_ranks(np.stack(parts), np.stack(lses))
+    _close(o, o_ref)
+    _close(lse, lse_ref)
+
+
+def test_dcp_single_rank_is_the_plain_decode():
+    inp = gen.dense_inputs(3, 3, 2, [10, 2, 5], seed=71)
+    o_ref, lse_ref = oracle.dense_decode(inp)
+    o, lse = oracle.dcp_decode(inp, inp.seq_lens.clone(), 0, 1)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(lse, lse_ref)
+
+
+@pytest.mark.parametrize("q_len,world", [(1, 2), (4, 3), (2, 5)])
+def test_dcp_share_matches_brute_force(q_len, world):
+    inp = gen.dense_inputs(2, q_len, 2, [9, 4], seed=81 + q_len, d_v=16, d_rope=8,
+                           extra_slots=2)
+    for k in range(world):
+        shard, glen = oracle.dcp_shard(inp, k, world)
+        o, lse = oracle.dcp_decode(shard, glen, k, world)
+        ob, lb = oracle.brute_force_dcp(inp, k, world)
+        _close(o, ob)
+        _close(lse, lb)
+
+
+def test_dcp_rank_without_visible_keys_gives_zero_and_minus_inf():
+    # global length 2 with q_len 2: row 0 sees position 0 only, so rank 1 of 2
+    # (positions 1, 3, ...) has nothing for row 0 and position 1 for row 1
+    inp = gen.dense_inputs(1, 2, 2, [2], seed=91)
+    shard, glen = oracle.dcp_shard(inp, 1, 2)
+    o, lse = oracle.dcp_decode(shard, glen, 1, 2)
+    assert np.all(o[0] == 0.0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(lse[1]))

@@ -70,6 +70,10 @@ extern "C" {
 #define MLA_DEVERR_TIMEOUT 2u        /* a bounded pipeline wait ran out: CTA gave up */
 #define MLA_DEVERR_BAD_LENGTH 4u     /* seq_lens[b] outside [0, kv_indptr[b+1]-kv_indptr[b]] */
 
+/* Element types of the DCP share buffers (mla_decode_dcp, mla_dcp_lse_merge_ranks). */
+#define MLA_DTYPE_BF16 0
+#define MLA_DTYPE_F32 1
+
 /* Largest split count the reducer accepts (hip_mha_decoding_num_partitions: the
  * reducer's 256-partition specialization caps the MLA-style split count). */
 #define MLA_MAX_SPLITS 256
@@ -167,6 +171,62 @@ int mla_sparse_decode(const mla_plan_t* plan, const void* q_nope, const void* q_
                       int32_t num_tokens, int32_t num_heads, int32_t topk, float scale,
                       float kv_scale, void* o, float* lse, void* workspace,
                       int64_t workspace_bytes, void* stream);
+
+/*
+ * Dense decode of one rank's share under decode context parallelism (DCP;
+ * moonmath-ai/amd-kernels README, "MLA absorbed decode" and "Use / MLA decode":
+ * one op serves plain decode, speculative verify and DCP; under DCP seq_lens
+ * counts this rank's positions, glen gives the global lengths, and the op
+ * returns a base-2 LSE for the cross-rank merge; "Constraints / MLA decode":
+ * DCP needs glen whenever cp_world > 1).
+ *   Rank cp_rank of cp_world holds the positions p of every request with
+ *   p % cp_world == cp_rank, in increasing order: its kv_indices/kv_indptr/
+ *   seq_lens list those positions' slots, so local key j is the global
+ *   position j * cp_world + cp_rank.
+ *   glen  int32 [batch] device: global lengths.  Draft row t of request b sees
+ *         the local keys j < seq_lens[b] with j * cp_world + cp_rank <=
+ *         glen[b] - q_len + t (the draft window of mla_decode in global
+ *         positions); a row that sees none gets o = 0, lse = -inf.
+ *   o     [batch*q_len, num_heads, 512]: the share's normalised output
+ *         (softmax over the rank's visible keys, times kv_scale), bf16 when
+ *         o_dtype is MLA_DTYPE_BF16 (the op's own output type, as in the
+ *         pages) or fp32 when MLA_DTYPE_F32 (no rounding before the merge, at
+ *         twice the exchange bytes); 16-byte aligned;
+ *   lse   fp32 [batch*q_len, num_heads] base 2 of the share, required when
+ *         cp_world > 1.
+ * cp_world in [1, MLA_MAX_SPLITS], cp_rank in [0, cp_world); glen and lse are
+ * required when cp_world > 1 (else MLA_ERR_INVALID_ARG), as is a known
+ * o_dtype.  With cp_world == 1, glen == NULL and MLA_DTYPE_BF16 the call is
+ * mla_decode.  The plan is mla_decode_plan's for the rank's own kv_indices
+ * length.  Other arguments as for mla_decode.
+ */
+int mla_decode_dcp(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+                   const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+                   const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+                   int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+                   const int32_t* glen, int32_t cp_rank, int32_t cp_world, int32_t o_dtype,
+                   void* o, float* lse, void* workspace, int64_t workspace_bytes,
+                   void* stream);
+
+/*
+ * Cross-rank merge of DCP shares (README, "Use / MLA decode":
+ * mla_dcp_lse_merge_ranks combines the ranks' outputs and base-2 LSEs after
+ * the all-to-all).  For each of `rows` rows, with k over the cp_world ranks:
+ *   M = max_k lse_in[k, row];  w_k = 2^(lse_in[k, row] - M)
+ *   out[row, :] = bf16(sum_k w_k parts_in[k, row, :] / sum_k w_k)
+ *   lse_out[row] = M + log2 sum_k w_k           (when lse_out is non-NULL)
+ * in the split-K reduce's fixed association (increasing k).  A row whose
+ * shares are all -inf gets out = 0 and lse_out = -inf.
+ *   parts_in [cp_world, rows, d_v] (rank-major, as an all-gather leaves it),
+ *            bf16 or fp32 as parts_dtype (MLA_DTYPE_BF16 / MLA_DTYPE_F32) says
+ *   lse_in   fp32 [cp_world, rows] base 2
+ *   out      bf16 [rows, d_v], written; lse_out fp32 [rows] or NULL
+ * d_v a multiple of 8 up to 512; cp_world in [1, MLA_MAX_SPLITS]; parts_in and
+ * out 16-byte aligned.  Device pointers; enqueued on `stream`.
+ */
+int mla_dcp_lse_merge_ranks(const void* parts_in, int32_t parts_dtype, const float* lse_in,
+                            int32_t cp_world, int64_t rows, int32_t d_v, void* out,
+                            float* lse_out, void* stream);
 
 /*
  * The two halves of mla_decode / mla_sparse_decode, for callers that keep the

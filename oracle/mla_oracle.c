@@ -315,15 +315,14 @@ int oracle_dcp_decode(int32_t batch, int32_t q_len, int32_t num_heads,
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < items; ++i) {
         int64_t r = i / num_heads;
-        int64_t h = i % num_heads;
         int64_t b = r / q_len;
         int64_t t = r % q_len;
         int64_t last = (int64_t)glen[b] - q_len + t;   /* last visible global position */
         int64_t n = 0;
         while (n < seq_lens[b] && n * cp_world + cp_rank <= last)
             ++n;
-        int local = attend_row(q_lat + (r * num_heads + h) * d_v,
-                               q_pe + (r * num_heads + h) * d_rope, d_v, d_rope,
+        /* item i is row r = i / num_heads, head h = i % num_heads */
+        int local = attend_row(q_lat + i * d_v, q_pe + i * d_rope, d_v, d_rope,
                                pool, pool_rows, kv_indices + kv_indptr[b], n,
                                scale, kv_scale, o + i * d_v, lse2 + i);
         if (local != ORACLE_OK) {

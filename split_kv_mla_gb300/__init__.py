@@ -4,11 +4,14 @@ hand-written for GB300 (sm_103a).
 The compute lives in ``libmla.so`` (CUDA kernels behind a C ABI, declared in
 ``include/mla_decode.h``); :mod:`split_kv_mla_gb300.mla` is the ctypes binding
 with the same entry-point names, and :mod:`split_kv_mla_gb300.inputs` draws the
-seeded synthetic workloads.
+seeded synthetic workloads.  :mod:`split_kv_mla_gb300.dcp` holds the host
+plumbing of decode context parallelism (rank page tables, the exchange step).
 """
 from .mla import (  # noqa: F401
     MlaError,
+    mla_dcp_lse_merge_ranks,
     mla_decode,
+    mla_decode_dcp,
     mla_decode_splits,
     mla_decode_plan,
     mla_plan_force_splits,

@@ -189,8 +189,9 @@ int run(const mla_plan_t* plan, SplitArgs& a, int64_t items, cudaStream_t stream
     cudaError_t e = launch_split_tc(a, *plan, stream);
     if (e != cudaSuccess) return MLA_ERR_LAUNCH_FAILED;
     if (with_reduce && plan->num_splits > 1) {
+        void* out = a.o_f32 ? static_cast<void*>(a.o_f32) : static_cast<void*>(a.o);
         e = launch_splitk_reduce(a.o_part, a.lse_part, items, plan->num_splits, plan->d_v,
-                                 a.out_scale, a.o, a.lse, stream);
+                                 a.out_scale, out, a.o_f32 != nullptr, a.lse, stream);
         if (e != cudaSuccess) return MLA_ERR_LAUNCH_FAILED;
     }
     return MLA_OK;
@@ -274,9 +275,12 @@ static int dense_call(const mla_plan_t* plan, const void* q_lat, const void* q_p
                       const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
                       int32_t q_len, int32_t num_heads, float scale, float kv_scale,
                       void* o_lat, float* lse, void* workspace, int64_t workspace_bytes,
-                      void* stream, bool with_reduce)
+                      void* stream, bool with_reduce, const int32_t* glen = nullptr,
+                      int32_t cp_rank = 0, int32_t cp_world = 1, bool o_f32 = false)
 {
     if (!plan) return MLA_ERR_INVALID_ARG;
+    if (cp_world < 1 || cp_world > MLA_MAX_SPLITS || cp_rank < 0 || cp_rank >= cp_world)
+        return MLA_ERR_INVALID_ARG;
     if (plan->batch != batch || plan->q_len != q_len || plan->num_heads != num_heads ||
         plan->d_v != kDenseDv || plan->d_rope != kDenseDr ||
         !variant_ok(plan) ||
@@ -285,6 +289,7 @@ static int dense_call(const mla_plan_t* plan, const void* q_lat, const void* q_p
     if (batch == 0) return MLA_OK;
     if (!q_lat || !q_pe || !pool || !seq_lens || !kv_indptr || !o_lat || pool_rows < 1)
         return MLA_ERR_INVALID_ARG;
+    if (cp_world > 1 && (!glen || !lse)) return MLA_ERR_INVALID_ARG;
     if (plan->total_keys > 0 && !kv_indices) return MLA_ERR_INVALID_ARG;
     if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(pool) || !aligned16(o_lat))
         return MLA_ERR_MISALIGNED;
@@ -313,9 +318,13 @@ static int dense_call(const mla_plan_t* plan, const void* q_lat, const void* q_p
     a.head_blocks = plan->head_blocks;
     a.logit_scale = scale * kv_scale * kLog2e;
     a.out_scale = kv_scale;
-    a.o = static_cast<uint16_t*>(o_lat);
+    a.o = o_f32 ? nullptr : static_cast<uint16_t*>(o_lat);
+    a.o_f32 = o_f32 ? static_cast<float*>(o_lat) : nullptr;
     a.lse = lse;
     a.sparse = 0;
+    a.glen = glen;
+    a.cp_rank = cp_rank;
+    a.cp_world = cp_world;
     const int64_t items = (int64_t)batch * q_len * num_heads;
     carve(plan, workspace, items, &a);
     return run(plan, a, items, static_cast<cudaStream_t>(stream), with_reduce);
@@ -396,6 +405,38 @@ int mla_decode_splits(const mla_plan_t* plan, const void* q_lat, const void* q_p
                       workspace_bytes, stream, false);
 }
 
+int mla_decode_dcp(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+                   const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+                   const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+                   int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+                   const int32_t* glen, int32_t cp_rank, int32_t cp_world, int32_t o_dtype,
+                   void* o, float* lse, void* workspace, int64_t workspace_bytes, void* stream)
+{
+    if (o_dtype != MLA_DTYPE_BF16 && o_dtype != MLA_DTYPE_F32) return MLA_ERR_INVALID_ARG;
+    return dense_call(plan, q_lat, q_pe, pool, pool_rows, seq_lens, kv_indices, kv_indptr,
+                      batch, q_len, num_heads, scale, kv_scale, o, lse, workspace,
+                      workspace_bytes, stream, true, glen, cp_rank, cp_world,
+                      o_dtype == MLA_DTYPE_F32);
+}
+
+int mla_dcp_lse_merge_ranks(const void* parts_in, int32_t parts_dtype, const float* lse_in,
+                            int32_t cp_world, int64_t rows, int32_t d_v, void* out,
+                            float* lse_out, void* stream)
+{
+    if (rows < 0 || cp_world < 1 || cp_world > MLA_MAX_SPLITS) return MLA_ERR_INVALID_ARG;
+    if (parts_dtype != MLA_DTYPE_BF16 && parts_dtype != MLA_DTYPE_F32) return MLA_ERR_INVALID_ARG;
+    if (d_v < 8 || (d_v % 8) != 0 || d_v > 4 * 128) return MLA_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MLA_OK;
+    if (!parts_in || !lse_in || !out) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(parts_in) || !aligned16(out)) return MLA_ERR_MISALIGNED;
+    int rc = device_ok();
+    if (rc != MLA_OK) return rc;
+    cudaError_t e = launch_dcp_merge(parts_in, parts_dtype == MLA_DTYPE_F32, lse_in, cp_world,
+                                     rows, d_v, static_cast<uint16_t*>(out), lse_out,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH_FAILED;
+}
+
 int mla_sparse_decode(const mla_plan_t* plan, const void* q_nope, const void* q_pe,
                       const void* pool, int64_t pool_rows, const int32_t* indices,
                       int32_t num_tokens, int32_t num_heads, int32_t topk, float scale,
@@ -440,9 +481,8 @@ int mla_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
     if (!std::isfinite(out_scale)) return MLA_ERR_INVALID_ARG;
     int rc = device_ok();
     if (rc != MLA_OK) return rc;
-    cudaError_t e = launch_splitk_reduce(o_part, lse_part, rows, num_splits, d_v, out_scale,
-                                         static_cast<uint16_t*>(o), lse,
-                                         static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_splitk_reduce(o_part, lse_part, rows, num_splits, d_v, out_scale, o,
+                                         false, lse, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH_FAILED;
 }
 

@@ -26,11 +26,17 @@ struct SplitArgs {
     float logit_scale;          // scale * kv_scale * log2(e): raw fp8 dot -> base-2 logit
     float out_scale;            // kv_scale: raw fp8 V units -> output units
     uint16_t* o;                // bf16 [rows, H, d_v]   (written when num_splits == 1)
+    float* o_f32;               // fp32 [rows, H, d_v] instead of o, or NULL
     float* lse;                 // fp32 [rows, H] or NULL
     float* o_part;              // fp32 [rows*H, ns, d_v] (num_splits > 1)
     float* lse_part;            // fp32 [rows*H, ns]
     uint32_t* err;              // workspace error word
     int sparse;
+    // decode context parallelism (dense only): local key i is global position
+    // i * cp_world + cp_rank; glen [batch] global lengths, or NULL to use seq_lens
+    const int32_t* glen = nullptr;
+    int32_t cp_rank = 0;
+    int32_t cp_world = 1;
 };
 
 // Kernel variants (mla_plan_t::variant).  Value 1 belonged to a CUDA-core
@@ -46,12 +52,18 @@ cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStre
 bool make_row_map(CUtensorMap* m, const void* pool, int64_t rows, int row_bytes, int box,
                   CUtensorMapSwizzle sw);
 
+// Merge of decode-context-parallel ranks' bf16 shares (mla_dcp_lse_merge_ranks).
+cudaError_t launch_dcp_merge(const void* parts, bool parts_f32, const float* lse_in,
+                             int32_t world, int64_t rows, int32_t d_v, uint16_t* o, float* lse,
+                             cudaStream_t stream);
+
 // Gather probe (mla_debug_gather).
 cudaError_t launch_gather_probe(const void* pool, int64_t pool_rows, int32_t row_bytes,
                                 const int32_t* indices, int64_t n, uint8_t* out, uint32_t* err,
                                 cudaStream_t stream);
+// Split-K reduce; writes o as bf16, or as fp32 when out_f32.
 cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
-                                 int32_t num_splits, int32_t d_v, float out_scale,
-                                 uint16_t* o, float* lse, cudaStream_t stream);
+                                 int32_t num_splits, int32_t d_v, float out_scale, void* o,
+                                 bool out_f32, float* lse, cudaStream_t stream);
 
 }  // namespace mla

@@ -22,17 +22,17 @@
 namespace mla {
 
 // One full warp: M, the weights w_s (written to w[0..ns)) and their sum for the
-// row whose LSEs are lse[0..ns), ns <= MLA_MAX_SPLITS.  Each lane loads its
-// LSEs once (s = lane + 32 k) and keeps them in registers.
+// row whose LSEs are lse[s * stride], s < ns <= MLA_MAX_SPLITS.  Each lane
+// loads its LSEs once (s = lane + 32 k) and keeps them in registers.
 __device__ __forceinline__ void merge_weights(const float* lse, int ns, float* w, float& m_out,
-                                              float& wsum_out, int lane)
+                                              float& wsum_out, int lane, int64_t stride = 1)
 {
     constexpr int kPer = MLA_MAX_SPLITS / 32;
     float l[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
         const int s = lane + 32 * k;
-        l[k] = s < ns ? __ldcg(lse + s) : -CUDART_INF_F;
+        l[k] = s < ns ? __ldcg(lse + s * stride) : -CUDART_INF_F;
     }
     float m = l[0];
 #pragma unroll

@@ -26,10 +26,21 @@ namespace {
 constexpr int kReduceThreads = 128;
 constexpr int kPrefetch = 16;
 
+// Four merged columns scaled by f, stored as bf16 or fp32.
+__device__ __forceinline__ void store4(__nv_bfloat16* o, float4 acc, float f)
+{
+    *reinterpret_cast<uint2*>(o) = merge_pack_bf16(acc, f);
+}
+__device__ __forceinline__ void store4(float* o, float4 acc, float f)
+{
+    *reinterpret_cast<float4*>(o) = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+}
+
+template <typename OutT>
 __global__ void __launch_bounds__(kReduceThreads)
 splitk_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                      int64_t rows, int num_splits, int d_v, float out_scale,
-                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse)
+                     OutT* __restrict__ o, float* __restrict__ lse)
 {
     __shared__ float w_s[MLA_MAX_SPLITS];
     __shared__ float fscale;
@@ -70,15 +81,92 @@ splitk_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__
             }
         }
         if (num_splits > kPrefetch) acc = merge_columns<8>(op, d_v, kPrefetch, num_splits, w_s, acc);
-        *reinterpret_cast<uint2*>(o + row * d_v + c) = merge_pack_bf16(acc, fscale);
+        store4(o + row * d_v + c, acc, fscale);
     }
+}
+
+// Four columns of a share as fp32, from bf16 (8 bytes) or fp32 (16 bytes).
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p)
+{
+    const uint2 x = __ldcg(reinterpret_cast<const uint2*>(p));
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ float4 load4(const float* p)
+{
+    return __ldcg(reinterpret_cast<const float4*>(p));
+}
+
+// Decode-context-parallel merge of the ranks' shares (rank-major
+// [world, rows, d_v], as an all-gather or all-to-all leaves them; bf16 or fp32)
+// with their base-2 LSEs [world, rows]: the same weights and fixed association
+// as the split-K reduce, the ranks taking the place of the splits.  One CTA per
+// row, four columns per thread.
+template <typename PartT>
+__global__ void __launch_bounds__(kReduceThreads)
+dcp_merge_kernel(const PartT* __restrict__ parts, const float* __restrict__ lse_in,
+                 int64_t rows, int world, int d_v, __nv_bfloat16* __restrict__ o,
+                 float* __restrict__ lse)
+{
+    __shared__ float w_s[MLA_MAX_SPLITS];
+    __shared__ float fscale;
+
+    const int64_t row = blockIdx.x;
+    if (row >= rows) return;
+    const int tid = threadIdx.x;
+    const int c = tid * 4;
+    const bool cols = c < d_v;
+    const int64_t rank_stride = rows * (int64_t)d_v;
+    const PartT* op = parts + row * d_v + c;
+    float4 v[kPrefetch];
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u)
+        if (cols && u < world) v[u] = load4(op + u * rank_stride);
+    if (tid < 32) {
+        float m, wsum;
+        merge_weights(lse_in + row, world, w_s, m, wsum, tid, rows);
+        if (tid == 0) {
+            fscale = wsum > 0.f ? 1.f / wsum : 0.f;
+            if (lse != nullptr) lse[row] = wsum > 0.f ? m + log2f(wsum) : -CUDART_INF_F;
+        }
+    }
+    __syncthreads();
+    if (!cols) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float ws, float4 x) {
+        acc.x += ws * x.x;
+        acc.y += ws * x.y;
+        acc.z += ws * x.z;
+        acc.w += ws * x.w;
+    };
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u)
+        if (u < world) add(w_s[u], v[u]);
+    for (int k = kPrefetch; k < world; ++k) add(w_s[k], load4(op + k * rank_stride));
+    store4(o + row * d_v + c, acc, fscale);
 }
 
 }  // namespace
 
+cudaError_t launch_dcp_merge(const void* parts, bool parts_f32, const float* lse_in,
+                             int32_t world, int64_t rows, int32_t d_v, uint16_t* o, float* lse,
+                             cudaStream_t stream)
+{
+    if (rows <= 0) return cudaSuccess;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(o);
+    if (parts_f32)
+        dcp_merge_kernel<float><<<(unsigned)rows, kReduceThreads, 0, stream>>>(
+            static_cast<const float*>(parts), lse_in, rows, world, d_v, out, lse);
+    else
+        dcp_merge_kernel<__nv_bfloat16><<<(unsigned)rows, kReduceThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(parts), lse_in, rows, world, d_v, out, lse);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
-                                 int32_t num_splits, int32_t d_v, float out_scale,
-                                 uint16_t* o, float* lse, cudaStream_t stream)
+                                 int32_t num_splits, int32_t d_v, float out_scale, void* o,
+                                 bool out_f32, float* lse, cudaStream_t stream)
 {
     if (rows <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
@@ -91,8 +179,11 @@ cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, o_part, lse_part, rows, num_splits, d_v,
-                              out_scale, reinterpret_cast<__nv_bfloat16*>(o), lse);
+    if (out_f32)
+        return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<float>, o_part, lse_part, rows,
+                                  num_splits, d_v, out_scale, static_cast<float*>(o), lse);
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<__nv_bfloat16>, o_part, lse_part, rows,
+                              num_splits, d_v, out_scale, static_cast<__nv_bfloat16*>(o), lse);
 }
 
 }  // namespace mla

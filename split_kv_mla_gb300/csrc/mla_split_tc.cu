@@ -355,6 +355,18 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             L = L < 0 ? 0 : cap;
         }
     }
+    // The draft window.  Local key i is the request's global position
+    // i * cp_world + cp_rank (decode context parallelism: this rank holds the
+    // positions p with p % cp_world == cp_rank; cp_world 1 otherwise), and draft
+    // row t sees the global positions up to G - q_len + t, G the request's global
+    // length (glen, or L itself).  win(t) is the number of local keys row t sees.
+    int G = L;
+    if (!SPARSE && a.glen != nullptr) G = a.glen[b];
+    auto window = [&](int t) {
+        const int x = G - a.q_len + t - a.cp_rank;
+        return x >= 0 ? x / a.cp_world + 1 : 0;
+    };
+    const int win_min = window(0);
     const int chunk = (L + a.num_splits - 1) / a.num_splits;
     const int k0 = min(L, split * chunk);
     const int k1 = min(L, k0 + chunk);
@@ -530,7 +542,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 const int idx = hb * N + n;
                 const bool valid = idx < rows_in_req;
                 ms.cq[n] = valid ? mul_pow2(a.logit_scale, -sh) : 0.f;
-                ms.win[n] = valid ? (L - a.q_len + idx / a.num_heads + 1) : -1;
+                ms.win[n] = valid ? window(idx / a.num_heads) : -1;
             }
         }
     }
@@ -717,9 +729,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             const int j = k0 + blk * kBlockN + ti;
             // Per-row logit scales and windows as 16-byte loads, and a
             // branch-free mask.  The draft window only bites in blocks that reach
-            // the last q_len - 1 positions of the request (kval already drops
-            // keys beyond the split).
-            const bool tail = k0 + (blk + 1) * kBlockN > L - a.q_len + 1;
+            // past the shortest row's window (kval already drops keys beyond
+            // the split).
+            const bool tail = k0 + (blk + 1) * kBlockN > win_min;
             const int jt = tail ? j : INT_MIN;
             bool need = false;
 #pragma unroll
@@ -879,7 +891,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
             for (int n = 0; n < R; ++n) inv[n] = 0.f;
         }
+        // One split writes the final rows: bf16 into o, or fp32 into o_f32 when
+        // the caller asked for fp32 output; several splits write fp32 partials.
         const bool final_rows = ns == 1;
+        const bool final16 = final_rows && a.o_f32 == nullptr;
+        const float fscale = final_rows ? a.out_scale : 1.f;
         float* ostage = reinterpret_cast<float*>(smem + C::kOffStage);              // fp32 [N][512]
         uint16_t* ostage16 = reinterpret_cast<uint16_t*>(smem + C::kOffStage);      // bf16 [N][512]
 #pragma unroll 1
@@ -892,14 +908,15 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
                 for (int n = 0; n < R; ++n) o[n] = 0.f;
             }
-            if (final_rows) {
+            if (final16) {
 #pragma unroll
                 for (int n = 0; n < R; ++n)
                     ostage16[(r0 + n) * 512 + c * 128 + ti] =
                         __bfloat16_as_ushort(__float2bfloat16_rn(o[n] * (inv[n] * a.out_scale)));
             } else {
 #pragma unroll
-                for (int n = 0; n < R; ++n) ostage[(r0 + n) * 512 + c * 128 + ti] = o[n] * inv[n];
+                for (int n = 0; n < R; ++n)
+                    ostage[(r0 + n) * 512 + c * 128 + ti] = o[n] * (inv[n] * fscale);
             }
         }
         fence_proxy_async_smem();
@@ -908,8 +925,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             const int row = r0 + ti;
             const long long item = ms.row_item[row];
             if (item >= 0) {
-                if (final_rows) {
+                if (final16) {
                     bulk_store(a.o + item * C::kDv, ostage16 + row * 512, C::kDv * 2);
+                    if (a.lse) a.lse[item] = ms.fin[1][row];
+                } else if (final_rows) {
+                    bulk_store(a.o_f32 + item * C::kDv, ostage + row * 512, C::kDv * 4);
                     if (a.lse) a.lse[item] = ms.fin[1][row];
                 } else {
                     bulk_store(a.o_part + (item * ns + split) * C::kDv, ostage + row * 512, C::kDv * 4);

@@ -94,6 +94,10 @@ def load(build_if_missing: bool = True):
             "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "mla_wave_fill_splits": (i32, [i32, i64, i32, i32, i32, i32, i32, i32, i32]),
             "mla_debug_gather": (ctypes.c_int, [vp, i64, i32, vp, i64, vp, vp, vp]),
+            "mla_decode_dcp": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, vp, i32, i32, i32,
+                                              f32, f32, vp, i32, i32, i32, vp, vp, vp, i64,
+                                              vp]),
+            "mla_dcp_lse_merge_ranks": (ctypes.c_int, [vp, i32, vp, i32, i64, i32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -214,6 +218,73 @@ def mla_decode(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv_ind
 def mla_decode_splits(*args, **kw):
     """Only the split kernel of mla_decode (see mla_workspace_partials)."""
     return mla_decode(*args, _entry="mla_decode_splits", **kw)
+
+
+_DTYPE_CODE = {torch.bfloat16: 0, torch.float32: 1}   # MLA_DTYPE_BF16, MLA_DTYPE_F32
+
+
+def mla_decode_dcp(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv_indptr,
+                   scale: float, kv_scale: float, glen, cp_rank: int, cp_world: int,
+                   o=None, lse=None, workspace_t=None, stream=None,
+                   out_dtype=torch.bfloat16):
+    """One decode-context-parallel rank's share; returns (o, lse).  The rank's
+    page table lists its positions p % cp_world == cp_rank; ``glen`` int32 [B]
+    holds the global lengths (may be None only when cp_world == 1).  The share
+    is bf16 (``out_dtype``, or the dtype of a given ``o``) or fp32."""
+    for name, t in (("q_lat", q_lat), ("q_pe", q_pe), ("pool", pool), ("seq_lens", seq_lens),
+                    ("kv_indices", kv_indices), ("kv_indptr", kv_indptr)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    if glen is not None and not glen.is_cuda:
+        raise ValueError("glen must be a CUDA tensor")
+    R, H = q_lat.shape[0], q_lat.shape[1]
+    batch = seq_lens.shape[0]
+    q_len = R // batch if batch else 1
+    if o is None:
+        o = torch.empty(q_lat.shape, dtype=out_dtype, device=q_lat.device)
+    if o.dtype not in _DTYPE_CODE:
+        raise ValueError("o must be bf16 or fp32")
+    if lse is None:
+        lse = torch.empty(R, H, dtype=torch.float32, device=q_lat.device)
+    if workspace_t is None:
+        workspace_t = workspace(plan, q_lat.device)
+    pool_u8 = pool.view(torch.uint8) if pool.dtype != torch.uint8 else pool
+    rc = load().mla_decode_dcp(
+        ctypes.byref(plan), _dev_ptr(q_lat, "q_lat", torch.bfloat16),
+        _dev_ptr(q_pe, "q_pe", torch.bfloat16), _dev_ptr(pool_u8, "pool"), pool_u8.shape[0],
+        _dev_ptr(seq_lens, "seq_lens", torch.int32), _dev_ptr(kv_indices, "kv_indices", torch.int32),
+        _dev_ptr(kv_indptr, "kv_indptr", torch.int32), batch, q_len, H, float(scale),
+        float(kv_scale), _dev_ptr(glen, "glen", torch.int32), int(cp_rank), int(cp_world),
+        _DTYPE_CODE[o.dtype], _dev_ptr(o, "o"), _dev_ptr(lse, "lse", torch.float32),
+        _dev_ptr(workspace_t, "workspace"), workspace_t.numel(), _stream_ptr(stream))
+    _check(rc, "mla_decode_dcp")
+    return o, lse
+
+
+def mla_dcp_lse_merge_ranks(parts_in, lse_in, out=None, lse_out=None, stream=None,
+                            return_lse: bool = True):
+    """Merge the ranks' shares: parts_in bf16 or fp32 [W, ...rows, d_v]
+    (rank-major), lse_in fp32 [W, ...rows]; returns (out bf16 [...rows, d_v],
+    lse_out fp32 [...rows])."""
+    if not parts_in.is_cuda or not lse_in.is_cuda:
+        raise ValueError("parts_in and lse_in must be CUDA tensors")
+    if parts_in.dtype not in _DTYPE_CODE:
+        raise ValueError("parts_in must be bf16 or fp32")
+    W, d_v = parts_in.shape[0], parts_in.shape[-1]
+    rows_shape = tuple(lse_in.shape[1:])
+    rows = lse_in[0].numel()
+    if parts_in[0].numel() != rows * d_v:
+        raise ValueError("parts_in and lse_in disagree on the rows")
+    if out is None:
+        out = torch.empty(rows_shape + (d_v,), dtype=torch.bfloat16, device=parts_in.device)
+    if lse_out is None and return_lse:
+        lse_out = torch.empty(rows_shape, dtype=torch.float32, device=parts_in.device)
+    rc = load().mla_dcp_lse_merge_ranks(
+        _dev_ptr(parts_in, "parts_in"), _DTYPE_CODE[parts_in.dtype],
+        _dev_ptr(lse_in, "lse_in", torch.float32), W, rows, d_v, _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(lse_out, "lse_out", torch.float32),
+        _stream_ptr(stream))
+    _check(rc, "mla_dcp_lse_merge_ranks")
+    return out, lse_out
 
 
 def mla_sparse_decode(plan: mla_plan_t, q_nope, q_pe, pool, indices, scale: float,

@@ -62,7 +62,26 @@ def make_workload(name: str):
     if name.startswith("p-"):
         b, s = (int(x) for x in name[2:].split("-"))
         return "dense", gen.workload_c1(q_len=4, seq=s, batch=b), f"B={b} H=16 q_len=4 S={s}"
+    if name.startswith("dcp") and "-" in name:
+        # rank 0's share of a dense workload under decode context parallelism
+        w, base = name[3:].split("-", 1)
+        kind, inp, desc = make_workload(base)
+        if kind != "dense" or int(w) < 2:
+            raise SystemExit("DCP applies to dense workloads over 2 or more ranks")
+        shard, glen = dcp_rank_inputs(inp, int(w), 0)
+        shard.dcp_glen, shard.dcp_world, shard.dcp_base = glen, int(w), inp
+        return "dcp", shard, f"{desc}, DCP rank 0 of {w}"
     raise SystemExit(f"unknown workload {name}")
+
+
+def dcp_rank_inputs(inp, world: int, rank: int = 0):
+    """(share inputs, glen): the rank's page table under DCP (positions
+    p % world == rank) over the same queries and pool."""
+    import dataclasses
+    from split_kv_mla_gb300 import dcp
+    sl, si, sp, glen = dcp.shard_page_table(inp.seq_lens, inp.kv_indices, inp.kv_indptr,
+                                            rank, world)
+    return dataclasses.replace(inp, seq_lens=sl, kv_indices=si, kv_indptr=sp), glen
 
 
 # The pages' MI300X results for the same dense shapes (H=16, q_len=4, shuffled
@@ -74,6 +93,8 @@ PAGES_MI300X_TBS = {(1, 150000): 1.13, (2, 150000): 1.54, (8, 8192): 0.73, (8, 3
 
 def pages_baseline_gbs(name: str):
     """The pages' GB/s for exactly this workload, or None."""
+    if name.startswith("dcp"):
+        return None
     if name == "c1q4":
         key = (8, 8192)
     elif name.startswith("p-"):
@@ -99,18 +120,22 @@ def job_gbs(bytes_per_call: int, world: int, ms_per_call: float) -> float:
 
 
 def keys_per_call(kind, inp) -> int:
-    if kind == "dense":
+    if kind in ("dense", "dcp"):
         return int(inp.seq_lens.sum())
     return int((inp.indices >= 0).sum())
 
 
 def kv_bytes_per_call(kind, inp) -> int:
-    return keys_per_call(kind, inp) * ROW_BYTES[kind]
+    return keys_per_call(kind, inp) * row_bytes(kind)
+
+
+def row_bytes(kind) -> int:
+    return ROW_BYTES["sparse" if kind == "sparse" else "dense"]
 
 
 def flops_per_call(kind, inp) -> int:
     # 2 * (QK width + V width) per key and query row
-    if kind == "dense":
+    if kind in ("dense", "dcp"):
         rows = inp.q_len * inp.num_heads
         return 2 * (576 + 512) * rows * keys_per_call(kind, inp)
     return 2 * (512 + 448) * inp.num_heads * keys_per_call(kind, inp)
@@ -244,26 +269,79 @@ class Runner:
 
     def plan_step(self):
         mla, inp = self.mla, self.inp
-        if self.kind == "dense":
+        if self.kind != "sparse":
             return mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads, inp.total_keys,
                                        self.sms)
         return mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, self.sms)
 
-    def step(self, i, stream, splits_only=False, plan=None):
-        mla, inp, d = self.mla, self.inp, self.copies[i % len(self.copies)]
+    def call(self, d, pool, o, lse, stream, splits_only=False, plan=None):
+        """One public call on the inputs `d` (pool given separately)."""
+        mla, inp = self.mla, self.inp
         plan = plan or self.plan_step()
         if self.kind == "dense":
             fn = mla.mla_decode_splits if splits_only else mla.mla_decode
-            fn(plan, d["q_lat"], d["q_pe"], d["pool"], d["seq_lens"], d["kv_indices"],
-               d["kv_indptr"], inp.scale, inp.kv_scale, o_lat=self.o, lse=self.lse,
+            fn(plan, d["q_lat"], d["q_pe"], pool, d["seq_lens"], d["kv_indices"],
+               d["kv_indptr"], inp.scale, inp.kv_scale, o_lat=o, lse=lse,
                workspace_t=self.ws, stream=stream)
         else:
             fn = mla.mla_sparse_decode_splits if splits_only else mla.mla_sparse_decode
-            fn(plan, d["q_nope"], d["q_pe"], d["pool"], d["indices"], inp.scale, inp.kv_scale,
-               o=self.o, lse=self.lse, workspace_t=self.ws, stream=stream)
+            fn(plan, d["q_nope"], d["q_pe"], pool, d["indices"], inp.scale, inp.kv_scale,
+               o=o, lse=lse, workspace_t=self.ws, stream=stream)
+
+    def step(self, i, stream, splits_only=False, plan=None):
+        d = self.copies[i % len(self.copies)]
+        self.call(d, d["pool"], self.o, self.lse, stream, splits_only, plan)
+
+    def input_names(self):
+        if self.kind == "sparse":
+            return ["q_nope", "q_pe", "indices"]
+        return ["q_lat", "q_pe", "seq_lens", "kv_indices", "kv_indptr"]
 
     def launches_per_step(self):
         return 1 if self.plan.num_splits == 1 else 2
+
+
+class DcpRunner(Runner):
+    """Rank 0's step under decode context parallelism, on one GPU: its share of
+    the workload (mla_decode_dcp, fp32 share) and the merge of all ranks'
+    shares (mla_dcp_lse_merge_ranks).  The other ranks' shares, which an
+    all-gather would deliver, are computed once beforehand and stay in place."""
+
+    def __init__(self, shard, device, copies):
+        super().__init__("dense", shard, device, copies)
+        self.kind = "dcp"
+        base_inp, world = shard.dcp_base, shard.dcp_world
+        self.world = world
+        self.glen = shard.dcp_glen.to(device)
+        rows, H = shard.batch * shard.q_len, shard.num_heads
+        self.parts = torch.zeros(world, rows, H, 512, dtype=torch.float32, device=device)
+        self.lses = torch.full((world, rows, H), -float("inf"), dtype=torch.float32,
+                               device=device)
+        mla = self.mla
+        for k in range(1, world):
+            sk, gk = dcp_rank_inputs(base_inp, world, k)
+            pk = mla.mla_decode_plan(sk.batch, sk.q_len, sk.num_heads, sk.total_keys, self.sms)
+            dk = {n: getattr(sk, n).to(device) for n in
+                  ("q_lat", "q_pe", "seq_lens", "kv_indices", "kv_indptr")}
+            mla.mla_decode_dcp(pk, dk["q_lat"], dk["q_pe"], self.copies[0]["pool"],
+                               dk["seq_lens"], dk["kv_indices"], dk["kv_indptr"], sk.scale,
+                               sk.kv_scale, gk.to(device), k, world, o=self.parts[k],
+                               lse=self.lses[k], workspace_t=mla.workspace(pk, device))
+        torch.cuda.synchronize(device)
+
+    def call(self, d, pool, o, lse, stream, splits_only=False, plan=None):
+        mla, inp = self.mla, self.inp
+        plan = plan or self.plan_step()
+        fn = mla.mla_decode_dcp_splits if splits_only else mla.mla_decode_dcp
+        fn(plan, d["q_lat"], d["q_pe"], pool, d["seq_lens"], d["kv_indices"], d["kv_indptr"],
+           inp.scale, inp.kv_scale, self.glen, 0, self.world, o=self.parts[0],
+           lse=self.lses[0], workspace_t=self.ws, stream=stream)
+        if not splits_only:
+            mla.mla_dcp_lse_merge_ranks(self.parts, self.lses, out=o, lse_out=lse,
+                                        stream=stream)
+
+    def launches_per_step(self):
+        return (1 if self.plan.num_splits == 1 else 2) + 1
 
     def copy_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.copies[0].values())
@@ -338,11 +416,8 @@ def e2e_measure(runner, stream, steps):
     (one copy of a packed buffer); the KV pool is resident cache state and
     rotates over the device copies like the main arm.  The steps are replayed
     from a CUDA graph, as a serving loop would."""
-    mla, inp = runner.mla, runner.inp
-    if runner.kind == "dense":
-        names = ["q_lat", "q_pe", "seq_lens", "kv_indices", "kv_indptr"]
-    else:
-        names = ["q_nope", "q_pe", "indices"]
+    inp = runner.inp
+    names = runner.input_names()
     src = [getattr(inp, n).contiguous() for n in names]
     host_in, host_views = _packed(src, pinned=True)
     for hv, t in zip(host_views, src):
@@ -358,15 +433,7 @@ def e2e_measure(runner, stream, steps):
 
     def one(i):
         dev_in.copy_(host_in, non_blocking=True)
-        pool = copies[i % len(copies)]["pool"]
-        if runner.kind == "dense":
-            mla.mla_decode(plan, d["q_lat"], d["q_pe"], pool, d["seq_lens"], d["kv_indices"],
-                           d["kv_indptr"], inp.scale, inp.kv_scale, o_lat=o, lse=lse,
-                           workspace_t=runner.ws, stream=stream)
-        else:
-            mla.mla_sparse_decode(plan, d["q_nope"], d["q_pe"], pool, d["indices"], inp.scale,
-                                  inp.kv_scale, o=o, lse=lse, workspace_t=runner.ws,
-                                  stream=stream)
+        runner.call(d, copies[i % len(copies)]["pool"], o, lse, stream, plan=plan)
         host_out.copy_(dev_out, non_blocking=True)
 
     n = len(copies)
@@ -397,7 +464,7 @@ def cpu_baseline(kind, inp, budget_s: float):
     whole requests (all heads and draft rows), repeated until about budget_s."""
     from oracle import oracle
     oracle.build()
-    if kind == "dense":
+    if kind != "sparse":
         n_req = inp.batch
         req_keys = inp.seq_lens.tolist()
         heads_rows = inp.q_len * inp.num_heads
@@ -422,8 +489,8 @@ def cpu_baseline(kind, inp, budget_s: float):
         if el >= budget_s or reps >= 100000:
             break
     keys = sum(req_keys[:n]) * reps
-    gbs = keys * ROW_BYTES[kind] / el / 1e9
-    sample = (f"{n} of {n_req} {'requests' if kind == 'dense' else 'tokens'} "
+    gbs = keys * row_bytes(kind) / el / 1e9
+    sample = (f"{n} of {n_req} {'tokens' if kind == 'sparse' else 'requests'} "
               f"(all {heads_rows} rows each), {reps} pass(es), {el:.1f} s")
     return {"value": gbs, "unit": "GB/s", "cores": oracle.cpu_threads(), "kind": "oracle",
             "sample": sample}
@@ -435,6 +502,15 @@ def _oracle_items(kind, inp, items):
     sel = np.asarray(items, dtype=np.int64)
     if kind == "dense":
         oracle.dense_decode(inp, sel)
+    elif kind == "dcp":
+        # items are the rows of the first n requests of rank 0's share
+        import dataclasses
+        n = len(items) // (inp.q_len * inp.num_heads)
+        end = int(inp.kv_indptr[n])
+        sub = dataclasses.replace(inp, batch=n, q_lat=inp.q_lat[:n * inp.q_len],
+                                  q_pe=inp.q_pe[:n * inp.q_len], seq_lens=inp.seq_lens[:n],
+                                  kv_indices=inp.kv_indices[:end], kv_indptr=inp.kv_indptr[:n + 1])
+        oracle.dcp_decode(sub, inp.dcp_glen[:n], 0, inp.dcp_world)
     else:
         oracle.sparse_decode(inp, sel)
 
@@ -449,11 +525,12 @@ def run_ours(args, rank, world, local_rank):
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     # rotation copies: total input bytes > 4x L2
     from split_kv_mla_gb300 import mla as _m  # noqa: F401
-    per_copy = (inp.pool.numel() + (inp.q_lat.numel() * 2 if kind == "dense" else inp.q_nope.numel() * 2)
-                + inp.q_pe.numel() * 2 + (inp.kv_indices.numel() * 4 if kind == "dense"
+    dense = kind != "sparse"
+    per_copy = (inp.pool.numel() + (inp.q_lat.numel() * 2 if dense else inp.q_nope.numel() * 2)
+                + inp.q_pe.numel() * 2 + (inp.kv_indices.numel() * 4 if dense
                                           else inp.indices.numel() * 4))
     copies = max(1, min(64, math.ceil(4 * l2 / max(per_copy, 1))))
-    runner = Runner(kind, inp, device, copies)
+    runner = DcpRunner(inp, device, copies) if kind == "dcp" else Runner(kind, inp, device, copies)
     stream = torch.cuda.Stream(device)
 
     # warm-up (eager) then graphs
@@ -521,7 +598,7 @@ def run_ours(args, rank, world, local_rank):
                         if pages_baseline_gbs(args.workload) else None),
         "dtype": "e4m3fn-kv/bf16-q/fp32-acc",
         "data": "synthetic (seeded; N(0,1) bf16 queries, N(0,1)/kv_scale e4m3fn pool, shuffled page_size-1 slots)",
-        "config": {"workload": f"{args.workload}: dense MLA decode {desc}" if kind == "dense"
+        "config": {"workload": f"{args.workload}: dense MLA decode {desc}" if dense
                    else f"{args.workload}: sparse top-k MLA decode {desc}",
                    "kv_bytes_per_call": bytes_call, "keys_per_call": keys_per_call(kind, inp),
                    "num_splits": runner.plan.num_splits, "head_blocks": runner.plan.head_blocks,
@@ -560,7 +637,7 @@ def run_reference(args, rank, world):
     oracle.build()
     kind, inp, desc = make_workload(args.workload)
     # one step = a bounded sample: the first request (all rows), fixed across steps
-    if kind == "dense":
+    if kind != "sparse":
         heads_rows = inp.q_len * inp.num_heads
         n_req = max(1, min(inp.batch, args.ref_requests))
         keys = int(inp.seq_lens[:n_req].sum())
@@ -576,8 +653,8 @@ def run_reference(args, rank, world):
         _oracle_items(kind, inp, items)
     el = time.perf_counter() - t0
     ms_step = el / args.steps * 1e3
-    value = keys * ROW_BYTES[kind] / (ms_step * 1e-3) / 1e9
-    sample = (f"{n_req} {'request' if kind == 'dense' else 'token'}(s) of the workload, "
+    value = keys * row_bytes(kind) / (ms_step * 1e-3) / 1e9
+    sample = (f"{n_req} {'token' if kind == 'sparse' else 'request'}(s) of the workload, "
               f"all {heads_rows} rows, per step")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",

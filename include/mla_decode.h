@@ -209,6 +209,20 @@ int mla_decode_dcp(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
                    void* stream);
 
 /*
+ * The split kernel of mla_decode_dcp alone (as mla_decode_splits is to
+ * mla_decode): with plan->num_splits == 1 it writes the share o / lse; with
+ * more it leaves the fp32 partials in the workspace for mla_splitk_reduce.
+ * Arguments as for mla_decode_dcp.
+ */
+int mla_decode_dcp_splits(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+                          const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+                          const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+                          int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+                          const int32_t* glen, int32_t cp_rank, int32_t cp_world,
+                          int32_t o_dtype, void* o, float* lse, void* workspace,
+                          int64_t workspace_bytes, void* stream);
+
+/*
  * Cross-rank merge of DCP shares (README, "Use / MLA decode":
  * mla_dcp_lse_merge_ranks combines the ranks' outputs and base-2 LSEs after
  * the all-to-all).  For each of `rows` rows, with k over the cp_world ranks:

@@ -419,6 +419,21 @@ int mla_decode_dcp(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
                       o_dtype == MLA_DTYPE_F32);
 }
 
+int mla_decode_dcp_splits(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
+                          const void* pool, int64_t pool_rows, const int32_t* seq_lens,
+                          const int32_t* kv_indices, const int32_t* kv_indptr, int32_t batch,
+                          int32_t q_len, int32_t num_heads, float scale, float kv_scale,
+                          const int32_t* glen, int32_t cp_rank, int32_t cp_world,
+                          int32_t o_dtype, void* o, float* lse, void* workspace,
+                          int64_t workspace_bytes, void* stream)
+{
+    if (o_dtype != MLA_DTYPE_BF16 && o_dtype != MLA_DTYPE_F32) return MLA_ERR_INVALID_ARG;
+    return dense_call(plan, q_lat, q_pe, pool, pool_rows, seq_lens, kv_indices, kv_indptr,
+                      batch, q_len, num_heads, scale, kv_scale, o, lse, workspace,
+                      workspace_bytes, stream, false, glen, cp_rank, cp_world,
+                      o_dtype == MLA_DTYPE_F32);
+}
+
 int mla_dcp_lse_merge_ranks(const void* parts_in, int32_t parts_dtype, const float* lse_in,
                             int32_t cp_world, int64_t rows, int32_t d_v, void* out,
                             float* lse_out, void* stream)

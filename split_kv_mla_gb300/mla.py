@@ -97,6 +97,9 @@ def load(build_if_missing: bool = True):
             "mla_decode_dcp": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, vp, i32, i32, i32,
                                               f32, f32, vp, i32, i32, i32, vp, vp, vp, i64,
                                               vp]),
+            "mla_decode_dcp_splits": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, vp, i32, i32,
+                                                     i32, f32, f32, vp, i32, i32, i32, vp, vp,
+                                                     vp, i64, vp]),
             "mla_dcp_lse_merge_ranks": (ctypes.c_int, [vp, i32, vp, i32, i64, i32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -226,7 +229,7 @@ _DTYPE_CODE = {torch.bfloat16: 0, torch.float32: 1}   # MLA_DTYPE_BF16, MLA_DTYP
 def mla_decode_dcp(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv_indptr,
                    scale: float, kv_scale: float, glen, cp_rank: int, cp_world: int,
                    o=None, lse=None, workspace_t=None, stream=None,
-                   out_dtype=torch.bfloat16):
+                   out_dtype=torch.bfloat16, _entry: str = "mla_decode_dcp"):
     """One decode-context-parallel rank's share; returns (o, lse).  The rank's
     page table lists its positions p % cp_world == cp_rank; ``glen`` int32 [B]
     holds the global lengths (may be None only when cp_world == 1).  The share
@@ -249,7 +252,7 @@ def mla_decode_dcp(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv
     if workspace_t is None:
         workspace_t = workspace(plan, q_lat.device)
     pool_u8 = pool.view(torch.uint8) if pool.dtype != torch.uint8 else pool
-    rc = load().mla_decode_dcp(
+    rc = getattr(load(), _entry)(
         ctypes.byref(plan), _dev_ptr(q_lat, "q_lat", torch.bfloat16),
         _dev_ptr(q_pe, "q_pe", torch.bfloat16), _dev_ptr(pool_u8, "pool"), pool_u8.shape[0],
         _dev_ptr(seq_lens, "seq_lens", torch.int32), _dev_ptr(kv_indices, "kv_indices", torch.int32),
@@ -257,8 +260,13 @@ def mla_decode_dcp(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv
         float(kv_scale), _dev_ptr(glen, "glen", torch.int32), int(cp_rank), int(cp_world),
         _DTYPE_CODE[o.dtype], _dev_ptr(o, "o"), _dev_ptr(lse, "lse", torch.float32),
         _dev_ptr(workspace_t, "workspace"), workspace_t.numel(), _stream_ptr(stream))
-    _check(rc, "mla_decode_dcp")
+    _check(rc, _entry)
     return o, lse
+
+
+def mla_decode_dcp_splits(*args, **kw):
+    """Only the split kernel of mla_decode_dcp (see mla_workspace_partials)."""
+    return mla_decode_dcp(*args, _entry="mla_decode_dcp_splits", **kw)
 
 
 def mla_dcp_lse_merge_ranks(parts_in, lse_in, out=None, lse_out=None, stream=None,

@@ -167,3 +167,21 @@ def test_dcp_rejections():
     bad = torch.zeros(2, 5, 100, dtype=torch.bfloat16, device="cuda")   # d_v not a multiple of 8
     with pytest.raises(mla.MlaError):
         mla.mla_dcp_lse_merge_ranks(bad, torch.zeros(2, 5, device="cuda"))
+
+
+def test_splits_then_reduce_equals_the_one_call():
+    inp = gen.dense_inputs(2, 4, 16, [3000, 900], seed=23, extra_slots=3)
+    d = _to_cuda(inp)
+    sl, si, sp, glen = dcp.shard_page_table(d["seq_lens"], d["kv_indices"], d["kv_indptr"], 1, 2)
+    plan = mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads, si.numel(), mla.sm_count())
+    plan = mla.mla_plan_force_splits(plan, 4)
+    args = (plan, d["q_lat"], d["q_pe"], d["pool"], sl, si, sp, inp.scale, inp.kv_scale,
+            glen, 1, 2)
+    ws = mla.workspace(plan)
+    o1, l1 = mla.mla_decode_dcp(*args, workspace_t=ws, out_dtype=torch.float32)
+    mla.mla_decode_dcp_splits(*args, workspace_t=ws, out_dtype=torch.float32)
+    op, lp = mla.mla_workspace_partials(plan, ws)
+    o2, l2 = mla.mla_splitk_reduce(op, lp, out_scale=inp.kv_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o1.reshape(o2.shape).to(torch.bfloat16))
+    assert torch.equal(l2, l1.reshape(-1))

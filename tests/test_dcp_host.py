@@ -107,3 +107,15 @@ def test_exchange_and_merge_world_size_2_gloo():
     for shape, o_err, l_err, fin_ok in res.values():
         assert shape == (2, 9, 2, 32)
         assert o_err <= 1e-12 and l_err <= 1e-12 and fin_ok
+
+
+def test_bench_dcp_workload_is_rank_0_share():
+    sys.path.insert(0, ROOT)
+    import bench
+    kind, inp, desc = bench.make_workload("dcp3-c0")
+    assert kind == "dcp" and "rank 0 of 3" in desc
+    assert inp.dcp_world == 3 and int(inp.dcp_glen[0]) == 256
+    assert inp.total_keys == 86                     # positions 0, 3, ..., 255
+    assert bench.kv_bytes_per_call(kind, inp) == 86 * 576
+    with pytest.raises(SystemExit):
+        bench.make_workload("dcp1-c0")

@@ -272,6 +272,25 @@ def dcp_merge_ranks(o_parts: np.ndarray, lse2_parts: np.ndarray) -> Tuple[np.nda
     return o.reshape(rows_shape + (d_v,)), lse.reshape(rows_shape)
 
 
+def sparse_extra_decode(inp) -> Tuple[np.ndarray, np.ndarray]:
+    """fp64 sparse decode over the main cache and a second (compressed) cache
+    (flashinfer cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits: ``extra_topk``
+    candidate slots per token in the second cache).  Token t attends the union
+    of its valid main candidates and its valid second-cache candidates in one
+    softmax: the two caches are laid end to end as one pool, the second cache's
+    slots shifted past the main pool's rows, and ``sparse_decode`` runs over the
+    joined candidate rows."""
+    n_main = inp.pool.shape[0]
+    pool = torch.cat([_u8(inp.pool).reshape(n_main, -1),
+                      _u8(inp.extra_pool).reshape(inp.extra_pool.shape[0], -1)], 0)
+    extra = inp.extra_indices.to(torch.int64)
+    shifted = torch.where(extra >= 0, extra + n_main, torch.full_like(extra, -1))
+    joined = torch.cat([inp.indices.to(torch.int64), shifted], 1).to(torch.int32)
+    one = dataclasses.replace(inp, pool=pool, indices=joined.contiguous(),
+                              topk=joined.shape[1], extra_pool=None, extra_indices=None)
+    return sparse_decode(one)
+
+
 def split_partials(q_lat, q_pe, pool, slots, scale, kv_scale,
                    num_splits: int) -> Tuple[np.ndarray, np.ndarray]:
     """Partials of one row over ``num_splits`` contiguous key ranges of equal

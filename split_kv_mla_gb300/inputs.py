@@ -76,6 +76,13 @@ class SparseInputs:
     indices: torch.Tensor    # int32 [T, topk]; negative = invalid entry
     scale: float
     kv_scale: float
+    # optional second (compressed) cache: same row format, own slot space
+    extra_pool: Optional[torch.Tensor] = None     # uint8 [N2, d_v + d_rope]
+    extra_indices: Optional[torch.Tensor] = None  # int32 [T, extra_topk]; negative = invalid
+
+    @property
+    def extra_topk(self) -> int:
+        return 0 if self.extra_indices is None else int(self.extra_indices.shape[1])
 
     @property
     def d_v(self) -> int:
@@ -170,6 +177,25 @@ def sparse_inputs(num_tokens: int, num_heads: int, topk: int, pool_rows: int,
         kv_scale=float(kv_scale))
 
 
+def sparse_extra_inputs(num_tokens: int, num_heads: int, topk: int, extra_topk: int,
+                        pool_rows: int, extra_rows: int, seed: int = 0, *,
+                        invalid_frac: float = 0.0, **kw) -> SparseInputs:
+    """``sparse_inputs(..., seed)`` plus a second cache of ``extra_rows`` rows
+    and per token ``extra_topk`` distinct slots of it, drawn from a second
+    generator (so the main part equals ``sparse_inputs`` with the same seed)."""
+    inp = sparse_inputs(num_tokens, num_heads, topk, pool_rows, seed,
+                        invalid_frac=invalid_frac, **kw)
+    g = _gen(seed + 7919)
+    inp.extra_pool = fp8_pool(extra_rows, inp.d_v + inp.d_rope, g, inp.kv_scale)
+    idx = torch.empty(num_tokens, extra_topk, dtype=torch.int32)
+    for t in range(num_tokens):
+        idx[t] = torch.randperm(extra_rows, generator=g)[:extra_topk].to(torch.int32)
+    if invalid_frac > 0:
+        idx[torch.rand(num_tokens, extra_topk, generator=g) < invalid_frac] = -1
+    inp.extra_indices = idx
+    return inp
+
+
 # --- the five synthetic workloads -------------------------------------------
 
 def workload_c0(seed: int = 0) -> DenseInputs:
@@ -199,3 +225,10 @@ def workload_c4(num_tokens: int, seed: int = 0, pool_rows: int = 131072,
                 topk: int = 2048) -> SparseInputs:
     """Sparse top-k: T tokens, 64 heads, 448+64 dims, top-k 2048 of 131072."""
     return sparse_inputs(num_tokens, 64, topk, pool_rows, seed)
+
+
+def workload_c4x(num_tokens: int, seed: int = 0, pool_rows: int = 131072, topk: int = 2048,
+                 extra_rows: int = 32768, extra_topk: int = 512) -> SparseInputs:
+    """Sparse top-k with a second (compressed) cache: the c4 shape plus, per
+    token, ``extra_topk`` candidates of a ``extra_rows``-row second cache."""
+    return sparse_extra_inputs(num_tokens, 64, topk, extra_topk, pool_rows, extra_rows, seed)

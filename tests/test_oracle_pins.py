@@ -362,3 +362,61 @@ def test_dcp_rank_without_visible_keys_gives_zero_and_minus_inf():
     o, lse = oracle.dcp_decode(shard, glen, 1, 2)
     assert np.all(o[0] == 0.0) and np.all(np.isneginf(lse[0]))
     assert np.all(np.isfinite(lse[1]))
+
+
+# ---- sparse decode with a second (compressed) cache ---------------------------------
+
+def _brute_force_sparse_extra(inp):
+    main = oracle._torch_decode_rows(inp.pool)
+    extra = oracle._torch_decode_rows(inp.extra_pool)
+    qn = inp.q_nope.to(torch.float64).tolist()
+    qp = inp.q_pe.to(torch.float64).tolist()
+    T, H = inp.num_tokens, inp.num_heads
+    o = np.zeros((T, H, inp.d_v))
+    lse = np.zeros((T, H))
+    for t in range(T):
+        rows = [main[s] for s in inp.indices[t].tolist() if s >= 0]
+        rows += [extra[s] for s in inp.extra_indices[t].tolist() if s >= 0]
+        for h in range(H):
+            o[t, h], lse[t, h] = oracle.brute_force_row(qn[t][h] + qp[t][h], rows, inp.d_v,
+                                                        inp.scale, inp.kv_scale)
+    return o, lse
+
+
+def test_sparse_extra_matches_brute_force():
+    inp = gen.sparse_extra_inputs(3, 2, 5, 3, pool_rows=12, extra_rows=7, seed=13,
+                                  invalid_frac=0.25, d_v=24, d_rope=8)
+    inp.indices[1, :] = -1              # a token whose candidates are all in the second cache
+    inp.extra_indices[2, :] = -1        # a token whose candidates are all in the main cache
+    o, lse = oracle.sparse_extra_decode(inp)
+    ob, lb = _brute_force_sparse_extra(inp)
+    _close(o, ob)
+    _close(lse, lb)
+
+
+def test_sparse_extra_with_no_valid_second_candidate_is_the_main_decode():
+    inp = gen.sparse_extra_inputs(4, 3, 16, 6, pool_rows=40, extra_rows=9, seed=17)
+    inp.extra_indices[:] = -1
+    o, lse = oracle.sparse_extra_decode(inp)
+    ro, rl = oracle.sparse_decode(inp)
+    np.testing.assert_array_equal(o, ro)
+    np.testing.assert_array_equal(lse, rl)
+
+
+def test_sparse_extra_equals_one_cache_holding_the_same_rows():
+    # the second cache holds copies of main-pool rows; pointing at the copies
+    # must equal listing the originals after the main candidates
+    inp = gen.sparse_extra_inputs(3, 2, 8, 5, pool_rows=30, extra_rows=5, seed=19)
+    src = torch.tensor([3, 17, 29, 0, 11])
+    inp.extra_pool = inp.pool[src].clone()
+    perm = torch.tensor([[4, 0, 2, 1, 3], [1, 1, 0, 4, 2], [3, -1, 2, 0, -1]], dtype=torch.int32)
+    inp.extra_indices = perm
+    o, lse = oracle.sparse_extra_decode(inp)
+    orig = torch.where(perm >= 0, src[perm.clamp(min=0).long()].to(torch.int32),
+                       torch.full_like(perm, -1))
+    one = gen.SparseInputs(num_tokens=3, num_heads=2, topk=13, q_nope=inp.q_nope, q_pe=inp.q_pe,
+                           pool=inp.pool, indices=torch.cat([inp.indices, orig], 1).contiguous(),
+                           scale=inp.scale, kv_scale=inp.kv_scale)
+    ro, rl = oracle.sparse_decode(one)
+    np.testing.assert_array_equal(o, ro)
+    np.testing.assert_array_equal(lse, rl)

@@ -59,6 +59,10 @@ def make_workload(name: str):
     if name.startswith("c4-"):
         t = int(name[3:])
         return "sparse", gen.workload_c4(t), f"T={t} H=64 top-k 2048 of 131072, 448+64"
+    if name.startswith("c4x-"):
+        t = int(name[4:])
+        return ("sparse", gen.workload_c4x(t),
+                f"T={t} H=64 top-k 2048 of 131072 + 512 of a 32768-row second cache, 448+64")
     if name.startswith("p-"):
         b, s = (int(x) for x in name[2:].split("-"))
         return "dense", gen.workload_c1(q_len=4, seq=s, batch=b), f"B={b} H=16 q_len=4 S={s}"
@@ -122,7 +126,8 @@ def job_gbs(bytes_per_call: int, world: int, ms_per_call: float) -> float:
 def keys_per_call(kind, inp) -> int:
     if kind in ("dense", "dcp"):
         return int(inp.seq_lens.sum())
-    return int((inp.indices >= 0).sum())
+    extra = int((inp.extra_indices >= 0).sum()) if inp.extra_topk else 0
+    return int((inp.indices >= 0).sum()) + extra
 
 
 def kv_bytes_per_call(kind, inp) -> int:
@@ -255,8 +260,11 @@ class Runner:
             self.o = torch.empty(rows, inp.num_heads, 512, dtype=torch.bfloat16, device=device)
             self.lse = torch.empty(rows, inp.num_heads, dtype=torch.float32, device=device)
         else:
-            self.plan = mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, sms)
+            self.plan = mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, sms,
+                                                   extra_topk=inp.extra_topk)
             base = dict(q_nope=inp.q_nope, q_pe=inp.q_pe, pool=inp.pool, indices=inp.indices)
+            if inp.extra_topk:
+                base.update(extra_pool=inp.extra_pool, extra_indices=inp.extra_indices)
             self.o = torch.empty(inp.num_tokens, inp.num_heads, 448, dtype=torch.bfloat16,
                                  device=device)
             self.lse = torch.empty(inp.num_tokens, inp.num_heads, dtype=torch.float32,
@@ -272,7 +280,8 @@ class Runner:
         if self.kind != "sparse":
             return mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads, inp.total_keys,
                                        self.sms)
-        return mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, self.sms)
+        return mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, self.sms,
+                                          extra_topk=inp.extra_topk)
 
     def call(self, d, pool, o, lse, stream, splits_only=False, plan=None):
         """One public call on the inputs `d` (pool given separately)."""
@@ -283,6 +292,11 @@ class Runner:
             fn(plan, d["q_lat"], d["q_pe"], pool, d["seq_lens"], d["kv_indices"],
                d["kv_indptr"], inp.scale, inp.kv_scale, o_lat=o, lse=lse,
                workspace_t=self.ws, stream=stream)
+        elif inp.extra_topk:
+            fn = mla.mla_sparse_decode_extra_splits if splits_only else mla.mla_sparse_decode_extra
+            fn(plan, d["q_nope"], d["q_pe"], pool, d["indices"], d["extra_pool"],
+               d["extra_indices"], inp.scale, inp.kv_scale, o=o, lse=lse, workspace_t=self.ws,
+               stream=stream)
         else:
             fn = mla.mla_sparse_decode_splits if splits_only else mla.mla_sparse_decode
             fn(plan, d["q_nope"], d["q_pe"], pool, d["indices"], inp.scale, inp.kv_scale,
@@ -294,7 +308,8 @@ class Runner:
 
     def input_names(self):
         if self.kind == "sparse":
-            return ["q_nope", "q_pe", "indices"]
+            return ["q_nope", "q_pe", "indices"] + (["extra_indices"] if self.inp.extra_topk
+                                                    else [])
         return ["q_lat", "q_pe", "seq_lens", "kv_indices", "kv_indptr"]
 
     def launches_per_step(self):
@@ -433,6 +448,8 @@ def e2e_measure(runner, stream, steps):
 
     def one(i):
         dev_in.copy_(host_in, non_blocking=True)
+        if "extra_pool" in copies[0]:
+            d["extra_pool"] = copies[i % len(copies)]["extra_pool"]
         runner.call(d, copies[i % len(copies)]["pool"], o, lse, stream, plan=plan)
         host_out.copy_(dev_out, non_blocking=True)
 
@@ -470,7 +487,10 @@ def cpu_baseline(kind, inp, budget_s: float):
         heads_rows = inp.q_len * inp.num_heads
     else:
         n_req = inp.num_tokens
-        req_keys = (inp.indices >= 0).sum(1).tolist()
+        req_keys = (inp.indices >= 0).sum(1)
+        if inp.extra_topk:
+            req_keys = req_keys + (inp.extra_indices >= 0).sum(1)
+        req_keys = req_keys.tolist()
         heads_rows = inp.num_heads
     # time one request, then size the sample
     t0 = time.perf_counter()
@@ -511,6 +531,13 @@ def _oracle_items(kind, inp, items):
                                   q_pe=inp.q_pe[:n * inp.q_len], seq_lens=inp.seq_lens[:n],
                                   kv_indices=inp.kv_indices[:end], kv_indptr=inp.kv_indptr[:n + 1])
         oracle.dcp_decode(sub, inp.dcp_glen[:n], 0, inp.dcp_world)
+    elif inp.extra_topk:
+        # items are the rows of the first n tokens
+        import dataclasses
+        n = len(items) // inp.num_heads
+        sub = dataclasses.replace(inp, num_tokens=n, q_nope=inp.q_nope[:n], q_pe=inp.q_pe[:n],
+                                  indices=inp.indices[:n], extra_indices=inp.extra_indices[:n])
+        oracle.sparse_extra_decode(sub)
     else:
         oracle.sparse_decode(inp, sel)
 
@@ -529,6 +556,8 @@ def run_ours(args, rank, world, local_rank):
     per_copy = (inp.pool.numel() + (inp.q_lat.numel() * 2 if dense else inp.q_nope.numel() * 2)
                 + inp.q_pe.numel() * 2 + (inp.kv_indices.numel() * 4 if dense
                                           else inp.indices.numel() * 4))
+    if not dense and inp.extra_topk:
+        per_copy += inp.extra_pool.numel() + inp.extra_indices.numel() * 4
     copies = max(1, min(64, math.ceil(4 * l2 / max(per_copy, 1))))
     runner = DcpRunner(inp, device, copies) if kind == "dcp" else Runner(kind, inp, device, copies)
     stream = torch.cuda.Stream(device)
@@ -645,6 +674,8 @@ def run_reference(args, rank, world):
         heads_rows = inp.num_heads
         n_req = max(1, min(inp.num_tokens, args.ref_requests))
         keys = int((inp.indices[:n_req] >= 0).sum())
+        if inp.extra_topk:
+            keys += int((inp.extra_indices[:n_req] >= 0).sum())
     items = list(range(n_req * heads_rows))
     for _ in range(args.warmup):
         _oracle_items(kind, inp, items)

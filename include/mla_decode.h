@@ -99,12 +99,13 @@ typedef struct {
                                 other values are rejected (MLA_ERR_INVALID_ARG) */
     int64_t workspace_bytes; /* bytes of device workspace the call needs */
     int32_t batch, q_len, num_heads, d_v, d_rope, sm_count;
-    int64_t total_keys;      /* dense: kv_indices length; sparse: tokens * topk */
+    int64_t total_keys;      /* dense: kv_indices length; sparse: tokens * (topk + extra_topk) */
     int32_t kv_share;        /* head blocks (CTAs) that share each gathered KV block
                                 through a thread-block cluster and TMA multicast:
                                 1, 2, 4 or 8, dividing head_blocks (1 when
                                 rows_per_cta is 16); results do not depend on it */
-    int32_t reserved;        /* 0 */
+    int32_t extra_topk;      /* sparse: candidates per token in the second
+                                (compressed) cache, 0 without one; dense: 0 */
 } mla_plan_t;
 
 /*
@@ -119,16 +120,18 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
 
 /*
  * Sparse top-k plan (flashinfer.mla.cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits:
- * one decode call's (num_splits, chunks per CTA) from tokens, heads, top-k and
- * the SM count; "[Perf] pa_decode_sparse ..." issue: 64 heads, 448 NoPE + 64
- * RoPE columns, top-k 2048).  d_v must be 448 and d_rope 64.  max_splits caps
- * num_splits (0 = MLA_MAX_SPLITS).  Every split count from 1 up is valid for
- * this kernel (a split may even be empty), so a small cap costs speed only and
- * is never an error.
+ * one decode call's (num_splits, chunks per CTA) from tokens, heads, top-k, the
+ * second cache's extra_topk and the SM count; "[Perf] pa_decode_sparse ..."
+ * issue: 64 heads, 448 NoPE + 64 RoPE columns, top-k 2048).  d_v must be 448
+ * and d_rope 64.  extra_topk = candidates per token in a second (compressed)
+ * cache, 0 without one (mla_sparse_decode_extra).  max_splits caps num_splits
+ * (0 = MLA_MAX_SPLITS).  Every split count from 1 up is valid for this kernel
+ * (a split may even be empty), so a small cap costs speed only and is never an
+ * error.
  */
 int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
-                           int32_t d_v, int32_t d_rope, int32_t sm_count, int32_t max_splits,
-                           mla_plan_t* out);
+                           int32_t extra_topk, int32_t d_v, int32_t d_rope, int32_t sm_count,
+                           int32_t max_splits, mla_plan_t* out);
 
 /*
  * Dense decode: enqueues the split kernel and, when plan->num_splits > 1, the
@@ -241,6 +244,38 @@ int mla_decode_dcp_splits(const mla_plan_t* plan, const void* q_lat, const void*
 int mla_dcp_lse_merge_ranks(const void* parts_in, int32_t parts_dtype, const float* lse_in,
                             int32_t cp_world, int64_t rows, int32_t d_v, void* out,
                             float* lse_out, void* stream);
+
+/*
+ * Sparse top-k decode over two caches in one call (flashinfer
+ * cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits: extra_topk candidate slots per
+ * token in the second (compressed) cache).  Token t attends, in one softmax,
+ * the valid entries of indices[t, 0:topk] (rows of pool) together with the
+ * valid entries of extra_indices[t, 0:extra_topk] (rows of extra_pool); a
+ * negative entry in either table is invalid and skipped, and a token with no
+ * valid entry gets o = 0, lse = -inf.
+ *   extra_pool    e4m3fn bytes [extra_rows, 512], the main pool's row format
+ *                 (448 NoPE + 64 RoPE columns) and kv_scale; 16-byte aligned
+ *   extra_indices int32 [num_tokens, extra_topk]
+ * The plan is mla_sparse_decode_plan's with the same topk and extra_topk.
+ * With extra_topk == 0 the call is mla_sparse_decode (extra_pool and
+ * extra_indices may be NULL).  Other arguments as for mla_sparse_decode.
+ */
+int mla_sparse_decode_extra(const mla_plan_t* plan, const void* q_nope, const void* q_pe,
+                            const void* pool, int64_t pool_rows, const int32_t* indices,
+                            const void* extra_pool, int64_t extra_rows,
+                            const int32_t* extra_indices, int32_t num_tokens, int32_t num_heads,
+                            int32_t topk, int32_t extra_topk, float scale, float kv_scale,
+                            void* o, float* lse, void* workspace, int64_t workspace_bytes,
+                            void* stream);
+/* The split kernel of mla_sparse_decode_extra alone (see mla_decode_splits). */
+int mla_sparse_decode_extra_splits(const mla_plan_t* plan, const void* q_nope,
+                                   const void* q_pe, const void* pool, int64_t pool_rows,
+                                   const int32_t* indices, const void* extra_pool,
+                                   int64_t extra_rows, const int32_t* extra_indices,
+                                   int32_t num_tokens, int32_t num_heads, int32_t topk,
+                                   int32_t extra_topk, float scale, float kv_scale, void* o,
+                                   float* lse, void* workspace, int64_t workspace_bytes,
+                                   void* stream);
 
 /*
  * The two halves of mla_decode / mla_sparse_decode, for callers that keep the

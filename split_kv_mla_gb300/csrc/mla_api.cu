@@ -251,22 +251,25 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
     return MLA_OK;
 }
 
-int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk, int32_t d_v,
-                           int32_t d_rope, int32_t sm_count, int32_t max_splits,
-                           mla_plan_t* out)
+int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
+                           int32_t extra_topk, int32_t d_v, int32_t d_rope, int32_t sm_count,
+                           int32_t max_splits, mla_plan_t* out)
 {
-    if (!out || num_tokens < 0 || topk < 0 || sm_count < 1 || max_splits < 0)
+    if (!out || num_tokens < 0 || topk < 0 || extra_topk < 0 || sm_count < 1 || max_splits < 0)
         return MLA_ERR_INVALID_ARG;
+    if ((int64_t)topk + extra_topk + 3 > (1LL << 30)) return MLA_ERR_UNSUPPORTED_SHAPE;
     if (d_v != kSparseDv || d_rope != kSparseDr || num_heads < 1 || num_heads > kMaxHeads)
         return MLA_ERR_UNSUPPORTED_SHAPE;
     const int32_t cap = max_splits == 0 ? MLA_MAX_SPLITS
                                         : (max_splits < MLA_MAX_SPLITS ? max_splits : MLA_MAX_SPLITS);
     const int64_t head_blocks = ceil_div(num_heads, rows_per_cta_for(num_heads));
-    int32_t ns = sparse_splits(head_blocks * (num_tokens > 0 ? num_tokens : 1), topk, sm_count);
+    int32_t ns = sparse_splits(head_blocks * (num_tokens > 0 ? num_tokens : 1),
+                               (int64_t)topk + extra_topk, sm_count);
     if (ns > cap) ns = cap;
     fill_plan(out, num_tokens, 1, num_heads, d_v, d_rope, sm_count,
-              (int64_t)num_tokens * topk, ns,
+              (int64_t)num_tokens * ((int64_t)topk + extra_topk), ns,
               kv_share_for(rows_per_cta_for(num_heads), head_blocks));
+    out->extra_topk = extra_topk;
     return MLA_OK;
 }
 
@@ -334,20 +337,25 @@ static int sparse_call(const mla_plan_t* plan, const void* q_nope, const void* q
                        const void* pool, int64_t pool_rows, const int32_t* indices,
                        int32_t num_tokens, int32_t num_heads, int32_t topk, float scale,
                        float kv_scale, void* o, float* lse, void* workspace,
-                       int64_t workspace_bytes, void* stream, bool with_reduce)
+                       int64_t workspace_bytes, void* stream, bool with_reduce,
+                       const void* extra_pool = nullptr, int64_t extra_rows = 0,
+                       const int32_t* extra_indices = nullptr, int32_t extra_topk = 0)
 {
     if (!plan) return MLA_ERR_INVALID_ARG;
+    if (topk < 0 || extra_topk < 0) return MLA_ERR_INVALID_ARG;
     if (plan->batch != num_tokens || plan->q_len != 1 || plan->num_heads != num_heads ||
         plan->d_v != kSparseDv || plan->d_rope != kSparseDr ||
-        !variant_ok(plan) ||
-        plan->total_keys != (int64_t)num_tokens * topk || plan->num_splits < 1 ||
-        plan->num_splits > MLA_MAX_SPLITS)
+        !variant_ok(plan) || plan->extra_topk != extra_topk ||
+        plan->total_keys != (int64_t)num_tokens * ((int64_t)topk + extra_topk) ||
+        plan->num_splits < 1 || plan->num_splits > MLA_MAX_SPLITS)
         return MLA_ERR_INVALID_ARG;
     if (num_tokens == 0) return MLA_OK;
-    if (!q_nope || !q_pe || !pool || !o || pool_rows < 1 || topk < 0)
-        return MLA_ERR_INVALID_ARG;
+    if (!q_nope || !q_pe || !pool || !o || pool_rows < 1) return MLA_ERR_INVALID_ARG;
     if (topk > 0 && !indices) return MLA_ERR_INVALID_ARG;
-    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(pool) || !aligned16(o))
+    if (extra_topk > 0 && (!extra_pool || !extra_indices || extra_rows < 1))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(pool) || !aligned16(o) ||
+        (extra_topk > 0 && !aligned16(extra_pool)))
         return MLA_ERR_MISALIGNED;
     if (!std::isfinite(scale) || !std::isfinite(kv_scale)) return MLA_ERR_INVALID_ARG;
     int rc = check_workspace(plan, workspace, workspace_bytes);
@@ -377,6 +385,12 @@ static int sparse_call(const mla_plan_t* plan, const void* q_nope, const void* q
     a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
     a.sparse = 1;
+    if (extra_topk > 0) {
+        a.extra_pool = static_cast<const uint8_t*>(extra_pool);
+        a.extra_rows = extra_rows;
+        a.extra_indices = extra_indices;
+        a.extra_topk = extra_topk;
+    }
     const int64_t items = (int64_t)num_tokens * num_heads;
     carve(plan, workspace, items, &a);
     return run(plan, a, items, static_cast<cudaStream_t>(stream), with_reduce);
@@ -460,6 +474,33 @@ int mla_sparse_decode(const mla_plan_t* plan, const void* q_nope, const void* q_
 {
     return sparse_call(plan, q_nope, q_pe, pool, pool_rows, indices, num_tokens, num_heads,
                        topk, scale, kv_scale, o, lse, workspace, workspace_bytes, stream, true);
+}
+
+int mla_sparse_decode_extra(const mla_plan_t* plan, const void* q_nope, const void* q_pe,
+                            const void* pool, int64_t pool_rows, const int32_t* indices,
+                            const void* extra_pool, int64_t extra_rows,
+                            const int32_t* extra_indices, int32_t num_tokens, int32_t num_heads,
+                            int32_t topk, int32_t extra_topk, float scale, float kv_scale,
+                            void* o, float* lse, void* workspace, int64_t workspace_bytes,
+                            void* stream)
+{
+    return sparse_call(plan, q_nope, q_pe, pool, pool_rows, indices, num_tokens, num_heads,
+                       topk, scale, kv_scale, o, lse, workspace, workspace_bytes, stream, true,
+                       extra_pool, extra_rows, extra_indices, extra_topk);
+}
+
+int mla_sparse_decode_extra_splits(const mla_plan_t* plan, const void* q_nope,
+                                   const void* q_pe, const void* pool, int64_t pool_rows,
+                                   const int32_t* indices, const void* extra_pool,
+                                   int64_t extra_rows, const int32_t* extra_indices,
+                                   int32_t num_tokens, int32_t num_heads, int32_t topk,
+                                   int32_t extra_topk, float scale, float kv_scale, void* o,
+                                   float* lse, void* workspace, int64_t workspace_bytes,
+                                   void* stream)
+{
+    return sparse_call(plan, q_nope, q_pe, pool, pool_rows, indices, num_tokens, num_heads,
+                       topk, scale, kv_scale, o, lse, workspace, workspace_bytes, stream, false,
+                       extra_pool, extra_rows, extra_indices, extra_topk);
 }
 
 int mla_sparse_decode_splits(const mla_plan_t* plan, const void* q_nope, const void* q_pe,

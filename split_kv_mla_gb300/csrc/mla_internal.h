@@ -32,6 +32,12 @@ struct SplitArgs {
     float* lse_part;            // fp32 [rows*H, ns]
     uint32_t* err;              // workspace error word
     int sparse;
+    // sparse only: a second (compressed) cache, extra_indices [tokens, extra_topk]
+    // into extra_pool [extra_rows, d_v + d_rope]; extra_topk 0 without one
+    const uint8_t* extra_pool = nullptr;
+    int64_t extra_rows = 0;
+    const int32_t* extra_indices = nullptr;
+    int32_t extra_topk = 0;
     // decode context parallelism (dense only): local key i is global position
     // i * cp_world + cp_rank; glen [batch] global lengths, or NULL to use seq_lens
     const int32_t* glen = nullptr;

@@ -341,11 +341,23 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
 
     // ---- the request's key list and this split's range --------------------------------
+    // Sparse with a second (compressed) cache: token b's keys are its topk main
+    // candidates, up to three invalid padding keys (so the second cache's keys
+    // start on a four-row group), then its extra_topk candidates in the second
+    // cache.  Splits then start on multiples of four keys, so every gather4
+    // group reads one cache.
     int64_t base;
     int L;
+    int topk4 = 0;
+    const int32_t* xlist = nullptr;
     if (SPARSE) {
         base = (int64_t)b * a.topk;
         L = a.topk;
+        if (a.extra_topk > 0) {
+            topk4 = (a.topk + 3) & ~3;
+            L = topk4 + a.extra_topk;
+            xlist = a.extra_indices + (int64_t)b * a.extra_topk;
+        }
     } else {
         base = a.kv_indptr[b];
         const int cap = a.kv_indptr[b + 1] - a.kv_indptr[b];
@@ -367,7 +379,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         return x >= 0 ? x / a.cp_world + 1 : 0;
     };
     const int win_min = window(0);
-    const int chunk = (L + a.num_splits - 1) / a.num_splits;
+    int chunk = (L + a.num_splits - 1) / a.num_splits;
+    if (SPARSE && a.extra_topk > 0) chunk = (chunk + 3) & ~3;
     const int k0 = min(L, split * chunk);
     const int k1 = min(L, k0 + chunk);
     const int nblk = (k1 - k0 + kBlockN - 1) / kBlockN;
@@ -390,13 +403,24 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     constexpr int kItemsPerWarp = (kItemsCta + kGatherWarps - 1) / kGatherWarps;
     static_assert(kItemsPerWarp <= 32, "one copy per lane");
     const int32_t* list = a.kv_indices + base;
+    const bool has_extra = SPARSE && a.extra_topk > 0;
+    // The index of key k of this request or token, and whether it lives in the
+    // second cache (-1: a padding key, invalid).
+    auto key_slot = [&](int k) -> int32_t {
+        if (!has_extra || k < a.topk) return __ldg(list + k);
+        return k < topk4 ? -1 : __ldg(xlist + (k - topk4));
+    };
+    auto key_extra = [&](int k) { return has_extra && k >= topk4; };
     const int cta_item = warp * kItemsPerWarp + lane;
     const bool item_on = warp < kGatherWarps && lane < kItemsPerWarp && cta_item < kItemsCta;
     const int my_item = rank * kItemsCta + cta_item;
     const int my_group = item_on ? my_item / kBoxes : 0;   // rows 4 g .. 4 g + 3
     const int my_box = item_on ? my_item % kBoxes : 0;
     const bool row_lane = tid < kBlockN;                   // warps 0-3: row tid's validity
-    struct Slots { int32_t v[4]; };
+    struct Slots {
+        int32_t v[4];
+        bool ex;   // the group's rows are in the second cache
+    };
     // The four indices of this lane's group in block j (-1 past the split),
     // and row tid's index.
     auto raw_slots = [&](int j) -> Slots {
@@ -406,20 +430,24 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int row = 4 * my_group + i;
-            r.v[i] = (item_on && row < nk) ? __ldg(list + kb + row) : -1;
+            r.v[i] = (item_on && row < nk) ? key_slot(kb + row) : -1;
         }
+        r.ex = key_extra(kb + 4 * my_group);
         return r;
     };
     auto raw_row = [&](int j) -> int32_t {
         const int kb = k0 + j * kBlockN;
         const int nk = min(kBlockN, k1 - kb);
-        return (row_lane && tid < nk) ? __ldg(list + kb + tid) : -1;
+        return (row_lane && tid < nk) ? key_slot(kb + tid) : -1;
     };
-    auto slot_ok = [&](int32_t v) { return v >= 0 && (int64_t)v < a.pool_rows; };
-    // Slots to gather: masked or invalid keys read pool row 0 (finite bytes, p = 0).
+    auto slot_ok = [&](int32_t v, bool ex) {
+        return v >= 0 && (int64_t)v < (ex ? a.extra_rows : a.pool_rows);
+    };
+    // Slots to gather: masked or invalid keys read row 0 of their cache
+    // (finite bytes, p = 0).
     auto fix_slots = [&](Slots r) -> Slots {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) r.v[i] = slot_ok(r.v[i]) ? r.v[i] : 0;
+        for (int i = 0; i < 4; ++i) r.v[i] = slot_ok(r.v[i], r.ex) ? r.v[i] : 0;
         return r;
     };
     // Validity of row tid (a dense slot out of range is reported, not read).
@@ -427,7 +455,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const int kb = k0 + j * kBlockN;
         const int nk = min(kBlockN, k1 - kb);
         if (!row_lane || tid >= nk) return 0;
-        if (slot_ok(v)) return 1;
+        if (slot_ok(v, key_extra(kb + tid))) return 1;
         if (!(SPARSE && v < 0) && rank == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
         return 0;
     };
@@ -448,7 +476,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             uint8_t* stage = smem + C::kOffStage + st * C::kStageBytes;
             uint8_t* dst = my_box < 4 ? stage + my_box * C::kLatChunkBytes + my_group * 512
                                       : stage + 4 * C::kLatChunkBytes + my_group * 256;
-            const CUtensorMap* map = my_box < 4 ? &tm_lat : &tm_rope;
+            // sparse: tm_rope is the second cache's map (512-byte rows, no RoPE box)
+            const CUtensorMap* map = (my_box < 4 && !sl.ex) ? &tm_lat : &tm_rope;
             const int x = my_box < 4 ? my_box * 128 : 512;
             if (CH > 1)
                 tma_gather4_multicast(dst, map, x, sl.v[0], sl.v[1], sl.v[2], sl.v[3],
@@ -459,12 +488,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     };
     Slots gnext{};
     int32_t rnext = -1;
-    Slots s0{{-1, -1, -1, -1}}, s1{{-1, -1, -1, -1}};
+    Slots s0{{-1, -1, -1, -1}, false}, s1{{-1, -1, -1, -1}, false};
     int32_t w0 = -1, w1 = -1;
     if (warp < kGatherWarps && nblk > 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tm_lat);
-            if (C::kRope) tma_prefetch_desc(&tm_rope);
+            if (C::kRope || has_extra) tma_prefetch_desc(&tm_rope);
         }
         // the index loads of blocks 0-2 are in flight together, during the set-up
         s0 = raw_slots(0);
@@ -1044,6 +1073,10 @@ cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStre
         return cudaErrorInvalidValue;
     if (!a.sparse) {
         if (!make_row_map(&rope, a.pool, a.pool_rows, row_bytes, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    } else if (a.extra_topk > 0) {
+        if (!make_row_map(&rope, a.extra_pool, a.extra_rows, row_bytes, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     } else {
         rope = lat;

@@ -47,7 +47,7 @@ class mla_plan_t(ctypes.Structure):
         ("batch", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_heads", ctypes.c_int32),
         ("d_v", ctypes.c_int32), ("d_rope", ctypes.c_int32), ("sm_count", ctypes.c_int32),
         ("total_keys", ctypes.c_int64), ("kv_share", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("extra_topk", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -74,7 +74,14 @@ def load(build_if_missing: bool = True):
         P = ctypes.POINTER(mla_plan_t)
         sig = {
             "mla_decode_plan": (ctypes.c_int, [i32, i32, i32, i64, i32, i32, i32, P]),
-            "mla_sparse_decode_plan": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, P]),
+            "mla_sparse_decode_plan": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, i32,
+                                                      P]),
+            "mla_sparse_decode_extra": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, i64, vp, i32,
+                                                       i32, i32, i32, f32, f32, vp, vp, vp, i64,
+                                                       vp]),
+            "mla_sparse_decode_extra_splits": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, i64, vp,
+                                                              i32, i32, i32, i32, f32, f32, vp,
+                                                              vp, vp, i64, vp]),
             "mla_decode": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, vp, i32, i32, i32, f32,
                                           f32, vp, vp, vp, i64, vp]),
             "mla_sparse_decode": (ctypes.c_int, [P, vp, vp, vp, i64, vp, i32, i32, i32, f32,
@@ -159,10 +166,12 @@ def mla_decode_plan(batch: int, q_len: int, num_heads: int, total_keys: int,
 
 
 def mla_sparse_decode_plan(num_tokens: int, num_heads: int, topk: int, sm_count: int,
-                           max_splits: int = 0, d_v: int = 448, d_rope: int = 64) -> mla_plan_t:
+                           max_splits: int = 0, d_v: int = 448, d_rope: int = 64,
+                           extra_topk: int = 0) -> mla_plan_t:
     p = mla_plan_t()
-    _check(load().mla_sparse_decode_plan(num_tokens, num_heads, topk, d_v, d_rope, sm_count,
-                                         max_splits, ctypes.byref(p)), "mla_sparse_decode_plan")
+    _check(load().mla_sparse_decode_plan(num_tokens, num_heads, topk, extra_topk, d_v, d_rope,
+                                         sm_count, max_splits, ctypes.byref(p)),
+           "mla_sparse_decode_plan")
     return p
 
 
@@ -319,6 +328,45 @@ def mla_sparse_decode(plan: mla_plan_t, q_nope, q_pe, pool, indices, scale: floa
         _dev_ptr(workspace_t, "workspace"), workspace_t.numel(), _stream_ptr(stream))
     _check(rc, _entry)
     return o, lse
+
+
+def mla_sparse_decode_extra(plan: mla_plan_t, q_nope, q_pe, pool, indices, extra_pool,
+                            extra_indices, scale: float, kv_scale: float, o=None, lse=None,
+                            workspace_t=None, stream=None, return_lse: bool = True,
+                            _entry: str = "mla_sparse_decode_extra"):
+    """Sparse top-k decode over the main cache and a second (compressed) cache
+    in one softmax: indices int32 [T, topk] into pool, extra_indices int32
+    [T, extra_topk] into extra_pool (both uint8 [N, 512]); returns (o, lse)."""
+    for name, t in (("q_nope", q_nope), ("q_pe", q_pe), ("pool", pool), ("indices", indices),
+                    ("extra_pool", extra_pool), ("extra_indices", extra_indices)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    topk = indices.shape[1] if indices.dim() == 2 else 0
+    extra_topk = extra_indices.shape[1] if extra_indices.dim() == 2 else 0
+    if o is None:
+        o = torch.empty_like(q_nope)
+    if lse is None and return_lse:
+        lse = torch.empty(T, H, dtype=torch.float32, device=q_nope.device)
+    if workspace_t is None:
+        workspace_t = workspace(plan, q_nope.device)
+    pool_u8 = pool.view(torch.uint8) if pool.dtype != torch.uint8 else pool
+    xpool_u8 = extra_pool.view(torch.uint8) if extra_pool.dtype != torch.uint8 else extra_pool
+    rc = getattr(load(), _entry)(
+        ctypes.byref(plan), _dev_ptr(q_nope, "q_nope", torch.bfloat16),
+        _dev_ptr(q_pe, "q_pe", torch.bfloat16), _dev_ptr(pool_u8, "pool"), pool_u8.shape[0],
+        _dev_ptr(indices, "indices", torch.int32), _dev_ptr(xpool_u8, "extra_pool"),
+        xpool_u8.shape[0], _dev_ptr(extra_indices, "extra_indices", torch.int32), T, H, topk,
+        extra_topk, float(scale), float(kv_scale), _dev_ptr(o, "o", torch.bfloat16),
+        _dev_ptr(lse, "lse", torch.float32), _dev_ptr(workspace_t, "workspace"),
+        workspace_t.numel(), _stream_ptr(stream))
+    _check(rc, _entry)
+    return o, lse
+
+
+def mla_sparse_decode_extra_splits(*args, **kw):
+    """Only the split kernel of mla_sparse_decode_extra."""
+    return mla_sparse_decode_extra(*args, _entry="mla_sparse_decode_extra_splits", **kw)
 
 
 def mla_sparse_decode_splits(*args, **kw):

@@ -235,6 +235,21 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 // One TMEM row of R query-row columns: hi columns at taddr_hi plus lo columns
 // at taddr_lo (the two halves of the stacked MMA output), summed.
+// The hi and lo columns of R rows, loads issued without waiting.
+template <int R>
+__device__ __forceinline__ void issue_rows(uint32_t taddr_hi, uint32_t taddr_lo,
+                                           uint32_t (&h)[R], uint32_t (&l)[R])
+{
+    static_assert(R == 8 || R == 16, "a softmax set holds 8 or 16 rows");
+    if constexpr (R == 16) {
+        tmem_ld16(taddr_hi, h);
+        tmem_ld16(taddr_lo, l);
+    } else {
+        tmem_ld8(taddr_hi, h);
+        tmem_ld8(taddr_lo, l);
+    }
+}
+
 template <int R>
 __device__ __forceinline__ void load_rows(uint32_t taddr_hi, uint32_t taddr_lo, float (&s)[R])
 {
@@ -910,16 +925,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const bool have_o = alive && nblk > 0 && warp_wait(&ms.o_done, 0, abort_flag);
         if (have_o) tc_fence_after();
         softmax_bar(bar_id);
-        float inv[R];
-        if (have_o) {
-            const uint32_t la = tmem + lane_addr + C::kColO + 4 * NC + r0;
-            load_rows<R>(la, la + N, inv);
-#pragma unroll
-            for (int n = 0; n < R; ++n) inv[n] = inv[n] > 0.f ? __frcp_rn(inv[n]) : 0.f;
-        } else {
-#pragma unroll
-            for (int n = 0; n < R; ++n) inv[n] = 0.f;
-        }
         // One split writes the final rows: bf16 into o, or fp32 into o_f32 when
         // the caller asked for fp32 output; several splits write fp32 partials.
         const bool final_rows = ns == 1;
@@ -927,26 +932,65 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const float fscale = final_rows ? a.out_scale : 1.f;
         float* ostage = reinterpret_cast<float*>(smem + C::kOffStage);              // fp32 [N][512]
         uint16_t* ostage16 = reinterpret_cast<uint16_t*>(smem + C::kOffStage);      // bf16 [N][512]
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            float o[R];
-            if (have_o) {
-                const uint32_t oa = tmem + lane_addr + C::kColO + c * NC + r0;
-                load_rows<R>(oa, oa + N, o);
-            } else {
-#pragma unroll
-                for (int n = 0; n < R; ++n) o[n] = 0.f;
-            }
+        // The sums and the four d_v chunks leave TMEM in two batches of loads
+        // (sums + chunks 0-1, then chunks 2-3), one wait each.
+        float scl[R];
+        auto stage_chunk = [&](int c, const uint32_t (&h)[R], const uint32_t (&l)[R]) {
             if (final16) {
 #pragma unroll
                 for (int n = 0; n < R; ++n)
-                    ostage16[(r0 + n) * 512 + c * 128 + ti] =
-                        __bfloat16_as_ushort(__float2bfloat16_rn(o[n] * (inv[n] * a.out_scale)));
+                    ostage16[(r0 + n) * 512 + c * 128 + ti] = __bfloat16_as_ushort(__float2bfloat16_rn(
+                        (__uint_as_float(h[n]) + __uint_as_float(l[n])) * scl[n]));
             } else {
 #pragma unroll
                 for (int n = 0; n < R; ++n)
-                    ostage[(r0 + n) * 512 + c * 128 + ti] = o[n] * (inv[n] * fscale);
+                    ostage[(r0 + n) * 512 + c * 128 + ti] =
+                        (__uint_as_float(h[n]) + __uint_as_float(l[n])) * scl[n];
             }
+        };
+        {
+            uint32_t sh[R], sl[R], h0[R], l0[R], h1[R], l1[R];
+            if (have_o) {
+                const uint32_t oa = tmem + lane_addr + C::kColO + r0;
+                issue_rows<R>(oa + 4 * NC, oa + 4 * NC + N, sh, sl);
+                issue_rows<R>(oa, oa + N, h0, l0);
+                issue_rows<R>(oa + NC, oa + NC + N, h1, l1);
+                tmem_wait_ld();
+                reg_fence(sh);
+                reg_fence(sl);
+                reg_fence(h0);
+                reg_fence(l0);
+                reg_fence(h1);
+                reg_fence(l1);
+            } else {
+#pragma unroll
+                for (int n = 0; n < R; ++n) sh[n] = sl[n] = h0[n] = l0[n] = h1[n] = l1[n] = 0u;
+            }
+#pragma unroll
+            for (int n = 0; n < R; ++n) {
+                const float lt = __uint_as_float(sh[n]) + __uint_as_float(sl[n]);
+                scl[n] = lt > 0.f ? rcp_approx(lt) * fscale : 0.f;
+            }
+            stage_chunk(0, h0, l0);
+            stage_chunk(1, h1, l1);
+        }
+        {
+            uint32_t h2[R], l2[R], h3[R], l3[R];
+            if (have_o) {
+                const uint32_t oa = tmem + lane_addr + C::kColO + r0;
+                issue_rows<R>(oa + 2 * NC, oa + 2 * NC + N, h2, l2);
+                issue_rows<R>(oa + 3 * NC, oa + 3 * NC + N, h3, l3);
+                tmem_wait_ld();
+                reg_fence(h2);
+                reg_fence(l2);
+                reg_fence(h3);
+                reg_fence(l3);
+            } else {
+#pragma unroll
+                for (int n = 0; n < R; ++n) h2[n] = l2[n] = h3[n] = l3[n] = 0u;
+            }
+            stage_chunk(2, h2, l2);
+            stage_chunk(3, h3, l3);
         }
         fence_proxy_async_smem();
         softmax_bar(bar_id);

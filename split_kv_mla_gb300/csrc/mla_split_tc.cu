@@ -275,7 +275,7 @@ __device__ __forceinline__ void load_rows(uint32_t taddr_hi, uint32_t taddr_lo, 
     }
 }
 
-template <int N, bool SPARSE, int CH>
+template <int N, bool SPARSE, int CH, bool EXTRA>
 __global__ void __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 const __grid_constant__ CUtensorMap tm_rope, const SplitArgs a)
@@ -368,7 +368,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     if (SPARSE) {
         base = (int64_t)b * a.topk;
         L = a.topk;
-        if (a.extra_topk > 0) {
+        if constexpr (EXTRA) {
             topk4 = (a.topk + 3) & ~3;
             L = topk4 + a.extra_topk;
             xlist = a.extra_indices + (int64_t)b * a.extra_topk;
@@ -395,7 +395,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     };
     const int win_min = window(0);
     int chunk = (L + a.num_splits - 1) / a.num_splits;
-    if (SPARSE && a.extra_topk > 0) chunk = (chunk + 3) & ~3;
+    if constexpr (EXTRA) chunk = (chunk + 3) & ~3;
     const int k0 = min(L, split * chunk);
     const int k1 = min(L, k0 + chunk);
     const int nblk = (k1 - k0 + kBlockN - 1) / kBlockN;
@@ -418,11 +418,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     constexpr int kItemsPerWarp = (kItemsCta + kGatherWarps - 1) / kGatherWarps;
     static_assert(kItemsPerWarp <= 32, "one copy per lane");
     const int32_t* list = a.kv_indices + base;
-    const bool has_extra = SPARSE && a.extra_topk > 0;
+    constexpr bool has_extra = EXTRA;   // only sparse launches have a second cache
     // The index of key k of this request or token, and whether it lives in the
     // second cache (-1: a padding key, invalid).
     auto key_slot = [&](int k) -> int32_t {
-        if (!has_extra || k < a.topk) return __ldg(list + k);
+        if (!has_extra) return __ldg(list + k);
+        if (k < a.topk) return __ldg(list + k);
         return k < topk4 ? -1 : __ldg(xlist + (k - topk4));
     };
     auto key_extra = [&](int k) { return has_extra && k >= topk4; };
@@ -1031,7 +1032,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
 // ---- host side -------------------------------------------------------------------------------
 
-template <int N, bool SPARSE, int CH>
+template <int N, bool SPARSE, int CH, bool EXTRA = false>
 cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
                            const mla_plan_t& plan, cudaStream_t stream)
 {
@@ -1039,7 +1040,7 @@ cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, cons
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(split_tc_kernel<N, SPARSE, CH>,
+        attr = cudaFuncSetAttribute(split_tc_kernel<N, SPARSE, CH, EXTRA>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr != cudaSuccess) return attr;
@@ -1062,17 +1063,17 @@ cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, cons
         la[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, split_tc_kernel<N, SPARSE, CH>, lat, rope, a);
+    return cudaLaunchKernelEx(&cfg, split_tc_kernel<N, SPARSE, CH, EXTRA>, lat, rope, a);
 }
 
-template <bool SPARSE>
+template <bool SPARSE, bool EXTRA = false>
 cudaError_t launch_rows32(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
                           const mla_plan_t& plan, cudaStream_t stream)
 {
     switch (plan.kv_share) {
-    case 2: return launch_variant<32, SPARSE, 2>(lat, rope, a, plan, stream);
-    case 4: return launch_variant<32, SPARSE, 4>(lat, rope, a, plan, stream);
-    default: return launch_variant<32, SPARSE, 1>(lat, rope, a, plan, stream);
+    case 2: return launch_variant<32, SPARSE, 2, EXTRA>(lat, rope, a, plan, stream);
+    case 4: return launch_variant<32, SPARSE, 4, EXTRA>(lat, rope, a, plan, stream);
+    default: return launch_variant<32, SPARSE, 1, EXTRA>(lat, rope, a, plan, stream);
     }
 }
 
@@ -1124,6 +1125,10 @@ cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStre
             return cudaErrorInvalidValue;
     } else {
         rope = lat;
+    }
+    if (a.sparse && a.extra_topk > 0) {
+        if (plan.rows_per_cta == 16) return launch_variant<16, true, 1, true>(lat, rope, a, plan, stream);
+        return launch_rows32<true, true>(lat, rope, a, plan, stream);
     }
     if (a.sparse) {
         if (plan.rows_per_cta == 16) return launch_variant<16, true, 1>(lat, rope, a, plan, stream);

@@ -44,8 +44,8 @@
 // * Sums.  Each block's exact fp32 p (for the LSE) is summed over the warp's
 //   32 keys with a transposing shuffle reduction, so each lane carries one row's
 //   running sum.  The sums of p_hi + p_lo (what the tensor core consumed, used
-//   to normalise O) come from the tensor core itself: a fifth P.V chunk whose A
-//   operand is an all-ones tile accumulates them next to O.
+//   to normalise O) are kept per thread and row across blocks (the split into
+//   e4m3 terms yields them) and reduced once, at the end.
 // * Safety.  Every mbarrier wait is time-bounded and warp-uniform; the softmax
 //   warps meet at bar.sync only at points every one of them reaches, and agree
 //   on giving up through the same barrier-reduction, so a stuck pipeline ends
@@ -100,22 +100,16 @@ struct Cfg {
     static constexpr int kOffStage = 0;
     static constexpr int kOffQ = 2 * kStageBytes;
     static constexpr int kOffP = kOffQ + kQBytes;
-    // An all-ones e4m3 tile (1.0 = 0x38) as the A operand of a fifth P.V chunk:
-    // its output is the column sums of P^T, i.e. the row sums of the p_hi + p_lo
-    // the tensor core consumed (any layout of a constant tile is the same tile).
-    static constexpr int kOffOnes = (kOffP + 2 * kPBytes + 1023) / 1024 * 1024;
-    static constexpr int kOnesBytes = kBlockN * 128;
-    static constexpr int kOffMisc = kOffOnes + kOnesBytes;
-    static constexpr uint32_t kTmemCols = (7 * NC <= 256) ? 256u : 512u;
+    static constexpr int kOffMisc = (kOffP + 2 * kPBytes + 127) / 128 * 128;
+    static constexpr uint32_t kTmemCols = (6 * NC <= 256) ? 256u : 512u;
     static constexpr uint32_t kColS = 0;                   // S^T buffers: [0, 2 NC)
-    static constexpr uint32_t kColO = 2 * NC;              // O^T chunks:  [2 NC, 6 NC), sums [6 NC, 7 NC)
+    static constexpr uint32_t kColO = 2 * NC;              // O^T chunks:  [2 NC, 6 NC)
     static constexpr int kGroups = kRowBytes / 8;          // 8-column query groups per row
     static constexpr int kVec = (kGroups + 31) / 32;       // query groups per lane
     static constexpr int kQRowsPerWarp = (N + kQWarps - 1) / kQWarps;
     static_assert(kOffQ % 1024 == 0 && kQChunkBytes % 1024 == 0, "128B-swizzle atoms");
     static_assert(kOffP % 16 == 0, "P tile alignment");
-    static_assert(7 * NC <= 512, "TMEM columns");
-    static_assert(kOffOnes % 1024 == 0, "ones tile alignment");
+    static_assert(6 * NC <= 512, "TMEM columns");
     static_assert(N * 512 * 4 <= 2 * kStageBytes, "epilogue staging fits in the stages");
 };
 
@@ -127,6 +121,7 @@ struct Misc {
     alignas(16) float cq[32];   // per query row: raw dot -> base-2 logit
     alignas(16) int win[32];   // per query row: keys at positions < win are visible
     float red[8][32];   // cross-warp reduction scratch, [set * 4 + warp of the set][row]
+    alignas(16) float redt[8][32];   // epilogue: the same for the consumed sums (p_hi + p_lo)
     alignas(16) float fin[2][32];   // epilogue: the base-2 LSE per row (fin[1])
     long long row_item[32];   // epilogue: output row (request row x head) per query row, -1 if none
 };
@@ -313,12 +308,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         mbar_init(&ms.o_done, 1);
         ms.abort = 0;
         fence_mbar_init();
-    }
-    {
-        uint4* ones = reinterpret_cast<uint4*>(smem + C::kOffOnes);
-        for (int i = tid; i < C::kOnesBytes / 16; i += kThreads)
-            ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
-        fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&ms.tmem_base, C::kTmemCols);
@@ -640,7 +629,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             const uint64_t qk_b_rope = smem_desc(qb + 4 * C::kQChunkBytes, 16, 512, kSw64);
             const uint64_t pv_a = smem_desc(stage0, C::kLatChunkBytes, 1024, kSw128);
             const uint64_t pv_b = smem_desc(smem_base + C::kOffP, 128, 2048, kSwNone);
-            const uint64_t pv_ones = smem_desc(smem_base + C::kOffOnes, C::kLatChunkBytes, 1024, kSw128);
             auto issue_pv = [&](int blk) {
                 const int st = blk & 1;
                 const uint64_t a0 = pv_a + (uint64_t)((st * C::kStageBytes) >> 4);
@@ -653,11 +641,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                 a0 + (uint64_t)((c * C::kLatChunkBytes + kk * 4096) >> 4),
                                 b0 + (uint64_t)((kk * 512) >> 4), id_pv,
                                 (blk > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_f8_warp(tmem + C::kColO + 4 * NC, pv_ones + (uint64_t)((kk * 4096) >> 4),
-                            b0 + (uint64_t)((kk * 512) >> 4), id_pv,
-                            (blk > 0 || kk > 0) ? 1u : 0u);
                 umma_commit_warp(&ms.pv_done[st]);
                 // the stage may be refilled once every CTA of the cluster is done
                 // with it (the last two blocks' stages are never refilled)
@@ -752,6 +735,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
         for (int n = 0; n < R; ++n) m_ref[n] = -CUDART_INF_F;
         float l_acc = 0.f;                                // running sum of row r0 + my_row over the warp's keys
+        float lt_acc[R];                                  // this thread's key: sums of p_hi + p_lo per row
+#pragma unroll
+        for (int n = 0; n < R; ++n) lt_acc[n] = 0.f;
         bool alive = true;
         for (int blk = 0; blk < nblk; ++blk) {
             const int st = blk & 1;
@@ -825,10 +811,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 for (int n = 0; n < R; ++n)
                     if (n == my_row) a_mine = alpha[n];
                 l_acc *= a_mine;
+#pragma unroll
+                for (int n = 0; n < R; ++n) lt_acc[n] *= alpha[n];
                 if (moved != 0 && blk > 0) {
                     // O^T holds blocks < blk: wait for the last P.V, then scale the
-                    // columns (hi and lo, four d_v chunks and the sums) of the rows
-                    // whose reference moved; the loop over rows is uniform.
+                    // columns (hi and lo, four d_v chunks) of the rows whose
+                    // reference moved; the loop over rows is uniform.
                     if (warp_wait(&ms.pv_done[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag)) {
                         tc_fence_after();
 #pragma unroll 1
@@ -839,9 +827,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
                             for (int k = 0; k < R; ++k)
                                 if (k == n) an = alpha[k];
-                            uint32_t rr[10];
+                            uint32_t rr[8];
 #pragma unroll
-                            for (int c = 0; c < 5; ++c) {
+                            for (int c = 0; c < 4; ++c) {
                                 const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + r0 + n;
                                 rr[2 * c] = tmem_ld1(ta);
                                 rr[2 * c + 1] = tmem_ld1(ta + N);
@@ -849,7 +837,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                             tmem_wait_ld();
                             reg_fence(rr);
 #pragma unroll
-                            for (int c = 0; c < 5; ++c) {
+                            for (int c = 0; c < 4; ++c) {
                                 const uint32_t ta = tmem + lane_addr + C::kColO + c * NC + r0 + n;
                                 tmem_st1(ta, __float_as_uint(__uint_as_float(rr[2 * c]) * an));
                                 tmem_st1(ta + N, __float_as_uint(__uint_as_float(rr[2 * c + 1]) * an));
@@ -872,8 +860,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                    ? 0.f : exp2f(x - m_ref[n + u] + kShift);
                 }
                 uint16_t h0, l0, h1, l1;
-                split_pair(s[n], s[n + 1], h0, l0);
-                split_pair(s[n + 2], s[n + 3], h1, l1);
+                const float2 t0 = split_pair(s[n], s[n + 1], h0, l0);
+                const float2 t1 = split_pair(s[n + 2], s[n + 3], h1, l1);
+                lt_acc[n] += t0.x;
+                lt_acc[n + 1] += t0.y;
+                lt_acc[n + 2] += t1.x;
+                lt_acc[n + 3] += t1.y;
                 hiw[n / 4] = (uint32_t)h0 | ((uint32_t)h1 << 16);
                 low[n / 4] = (uint32_t)l0 | ((uint32_t)l1 << 16);
             }
@@ -902,12 +894,18 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
         // ---- epilogue ------------------------------------------------------------------------
         // Row sums over all 128 keys -> the base-2 LSE per row (from the exact
-        // fp32 p), and each row's output index; the sums of what the MMA
-        // consumed (lt) sit in the fifth O chunk.  O^T leaves TMEM already
-        // normalised (times 1/lt, and kv_scale into bf16 for a single split)
-        // into the idle KV stages, and one bulk TMA store per row writes it out.
-        // Each set handles its own rows.
-        if ((lane % kLanesPerRow) == 0) red[sw * 32 + my_row] = l_acc;
+        // fp32 p), and each row's output index; the per-thread sums of what the
+        // MMA consumed (lt) are reduced over the set's keys the same way.  O^T
+        // leaves TMEM already normalised (times 1/lt, and kv_scale into bf16 for
+        // a single split) into the idle KV stages, and one bulk TMA store per
+        // row writes it out.  Each set handles its own rows.
+        {
+            const float t = warp_transpose_reduce<R, false>(lt_acc, lane);
+            if ((lane % kLanesPerRow) == 0) {
+                red[sw * 32 + my_row] = l_acc;
+                ms.redt[set * 4 + sw][my_row] = t;
+            }
+        }
         softmax_bar(bar_id);
         const int ns = a.num_splits;
         if (ti < R) {
@@ -933,9 +931,16 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const float fscale = final_rows ? a.out_scale : 1.f;
         float* ostage = reinterpret_cast<float*>(smem + C::kOffStage);              // fp32 [N][512]
         uint16_t* ostage16 = reinterpret_cast<uint16_t*>(smem + C::kOffStage);      // bf16 [N][512]
-        // The sums and the four d_v chunks leave TMEM in two batches of loads
-        // (sums + chunks 0-1, then chunks 2-3), one wait each.
+        // Row scale: 1 / (the consumed sum over all 128 keys of every block),
+        // times the output scale for final rows.  The four d_v chunks leave TMEM
+        // in two batches of loads (chunks 0-1, then 2-3), one wait each.
         float scl[R];
+#pragma unroll
+        for (int n = 0; n < R; ++n) {
+            const float lt = (ms.redt[set * 4][n] + ms.redt[set * 4 + 1][n]) +
+                             (ms.redt[set * 4 + 2][n] + ms.redt[set * 4 + 3][n]);
+            scl[n] = (have_o && lt > 0.f) ? rcp_approx(lt) * fscale : 0.f;
+        }
         auto stage_chunk = [&](int c, const uint32_t (&h)[R], const uint32_t (&l)[R]) {
             if (final16) {
 #pragma unroll
@@ -950,27 +955,19 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
         };
         {
-            uint32_t sh[R], sl[R], h0[R], l0[R], h1[R], l1[R];
+            uint32_t h0[R], l0[R], h1[R], l1[R];
             if (have_o) {
                 const uint32_t oa = tmem + lane_addr + C::kColO + r0;
-                issue_rows<R>(oa + 4 * NC, oa + 4 * NC + N, sh, sl);
                 issue_rows<R>(oa, oa + N, h0, l0);
                 issue_rows<R>(oa + NC, oa + NC + N, h1, l1);
                 tmem_wait_ld();
-                reg_fence(sh);
-                reg_fence(sl);
                 reg_fence(h0);
                 reg_fence(l0);
                 reg_fence(h1);
                 reg_fence(l1);
             } else {
 #pragma unroll
-                for (int n = 0; n < R; ++n) sh[n] = sl[n] = h0[n] = l0[n] = h1[n] = l1[n] = 0u;
-            }
-#pragma unroll
-            for (int n = 0; n < R; ++n) {
-                const float lt = __uint_as_float(sh[n]) + __uint_as_float(sl[n]);
-                scl[n] = lt > 0.f ? rcp_approx(lt) * fscale : 0.f;
+                for (int n = 0; n < R; ++n) h0[n] = l0[n] = h1[n] = l1[n] = 0u;
             }
             stage_chunk(0, h0, l0);
             stage_chunk(1, h1, l1);

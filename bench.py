@@ -66,6 +66,11 @@ def make_workload(name: str):
     if name.startswith("p-"):
         b, s = (int(x) for x in name[2:].split("-"))
         return "dense", gen.workload_c1(q_len=4, seq=s, batch=b), f"B={b} H=16 q_len=4 S={s}"
+    if name.startswith("d-"):
+        # any dense shape: d-B-H-Q-S (batch, heads, q_len, keys per request)
+        b, h, q, s = (int(x) for x in name[2:].split("-"))
+        return ("dense", gen.dense_inputs(b, q, h, [s] * b, 0),
+                f"B={b} H={h} q_len={q} S={s}")
     if name.startswith("dcp") and "-" in name:
         # rank 0's share of a dense workload under decode context parallelism
         w, base = name[3:].split("-", 1)
@@ -246,10 +251,11 @@ def recorded_traffic(workload: str):
 class Runner:
     """Device copies of one workload and the calls that run it."""
 
-    def __init__(self, kind, inp, device, copies):
+    def __init__(self, kind, inp, device, copies, force_splits=0):
         from split_kv_mla_gb300 import mla
         self.mla = mla
         self.kind, self.inp, self.device = kind, inp, device
+        self.force_splits = force_splits
         sms = mla.sm_count(device)
         if kind == "dense":
             self.plan = mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads,
@@ -269,6 +275,8 @@ class Runner:
                                  device=device)
             self.lse = torch.empty(inp.num_tokens, inp.num_heads, dtype=torch.float32,
                                    device=device)
+        if force_splits:
+            self.plan = mla.mla_plan_force_splits(self.plan, force_splits)
         first = {k: v.to(device) for k, v in base.items()}
         self.copies = [first] + [{k: v.clone() for k, v in first.items()}
                                  for _ in range(copies - 1)]
@@ -278,10 +286,12 @@ class Runner:
     def plan_step(self):
         mla, inp = self.mla, self.inp
         if self.kind != "sparse":
-            return mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads, inp.total_keys,
-                                       self.sms)
-        return mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, self.sms,
-                                          extra_topk=inp.extra_topk)
+            p = mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads, inp.total_keys,
+                                    self.sms)
+        else:
+            p = mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, self.sms,
+                                           extra_topk=inp.extra_topk)
+        return mla.mla_plan_force_splits(p, self.force_splits) if self.force_splits else p
 
     def call(self, d, pool, o, lse, stream, splits_only=False, plan=None):
         """One public call on the inputs `d` (pool given separately)."""
@@ -322,8 +332,8 @@ class DcpRunner(Runner):
     shares (mla_dcp_lse_merge_ranks).  The other ranks' shares, which an
     all-gather would deliver, are computed once beforehand and stay in place."""
 
-    def __init__(self, shard, device, copies):
-        super().__init__("dense", shard, device, copies)
+    def __init__(self, shard, device, copies, force_splits=0):
+        super().__init__("dense", shard, device, copies, force_splits)
         self.kind = "dcp"
         base_inp, world = shard.dcp_base, shard.dcp_world
         self.world = world
@@ -559,7 +569,8 @@ def run_ours(args, rank, world, local_rank):
     if not dense and inp.extra_topk:
         per_copy += inp.extra_pool.numel() + inp.extra_indices.numel() * 4
     copies = max(1, min(64, math.ceil(4 * l2 / max(per_copy, 1))))
-    runner = DcpRunner(inp, device, copies) if kind == "dcp" else Runner(kind, inp, device, copies)
+    runner = (DcpRunner(inp, device, copies, args.splits) if kind == "dcp"
+              else Runner(kind, inp, device, copies, args.splits))
     stream = torch.cuda.Stream(device)
 
     # warm-up (eager) then graphs
@@ -634,6 +645,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"inputs rotated over {copies} device copies "
                          f"({copies * per_copy / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
                    "timing": "CUDA-graph replays, CUDA events on the launch stream",
+                   **({"forced_splits": args.splits} if args.splits else {}),
                    "parallelism": f"replicas x{world}"},
         "us_per_call": ms_step * 1e3,
         "keys_per_s": keys_per_call(kind, inp) * world / (ms_step * 1e-3),
@@ -711,6 +723,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-requests", type=int, default=1)
+    ap.add_argument("--splits", type=int, default=0,
+                    help="force the split count instead of the planner's (split sweeps)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -106,6 +106,11 @@ typedef struct {
                                 rows_per_cta is 16); results do not depend on it */
     int32_t extra_topk;      /* sparse: candidates per token in the second
                                 (compressed) cache, 0 without one; dense: 0 */
+    int32_t long_first;      /* dense, 1: grid slice z serves the z-th longest
+                                request (ties by index), so the longest work is
+                                scheduled first; set when the grid outlasts one
+                                wave and batch <= 256; results do not depend on it */
+    int32_t reserved;        /* 0 */
 } mla_plan_t;
 
 /*

@@ -9,6 +9,9 @@
 namespace mla {
 
 // Parameters of one split-kernel launch (dense or sparse).
+// Largest batch for which the split kernel orders requests longest first.
+constexpr int kLongFirstMaxBatch = 256;
+
 struct SplitArgs {
     const uint16_t* q_lat;      // bf16 [rows, H, d_v]  (dense q_lat / sparse q_nope)
     const uint16_t* q_pe;       // bf16 [rows, H, d_rope]
@@ -38,6 +41,9 @@ struct SplitArgs {
     int64_t extra_rows = 0;
     const int32_t* extra_indices = nullptr;
     int32_t extra_topk = 0;
+    // dense only: grid slice z takes the z-th longest request (batch at most
+    // kLongFirstMaxBatch)
+    int32_t long_first = 0;
     // decode context parallelism (dense only): local key i is global position
     // i * cp_world + cp_rank; glen [batch] global lengths, or NULL to use seq_lens
     const int32_t* glen = nullptr;

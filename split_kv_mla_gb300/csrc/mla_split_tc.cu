@@ -124,6 +124,8 @@ struct Misc {
     alignas(16) float redt[8][32];   // epilogue: the same for the consumed sums (p_hi + p_lo)
     alignas(16) float fin[2][32];   // epilogue: the base-2 LSE per row (fin[1])
     long long row_item[32];   // epilogue: output row (request row x head) per query row, -1 if none
+    int lens[kLongFirstMaxBatch];   // longest-first ordering: the requests' lengths
+    int req;                        // longest-first ordering: this CTA's request
 };
 
 template <int N, bool SPARSE>
@@ -283,7 +285,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     volatile int* abort_flag = &ms.abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hb = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+    const int hb = blockIdx.x, split = blockIdx.y;
+    int b = blockIdx.z;   // the request (token); remapped below when long_first is set
     // Let a programmatic dependent (the split-K reduce) be scheduled as soon as
     // every CTA of this grid has started; it waits for this grid's completion
     // before reading anything.
@@ -318,6 +321,27 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     // still be writing the inputs (queries, page table, cache rows): wait for it
     // before the first global read.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // Longest requests first.  With more CTAs than one wave, grid slice z takes
+    // the z-th request in decreasing length order (ties in index order): the
+    // block scheduler hands out CTAs in index order, so the longest work starts
+    // first and the last wave holds the shortest (longest-processing-time
+    // ordering).  Every CTA derives the same permutation from seq_lens.
+    if (!SPARSE && a.long_first && a.batch <= kLongFirstMaxBatch) {
+        for (int t = tid; t < a.batch; t += kThreads) ms.lens[t] = a.seq_lens[t];
+        __syncthreads();
+        if (tid < a.batch) {
+            const int lt = ms.lens[tid];
+            int rank = 0;
+            for (int r = 0; r < a.batch; ++r) {
+                const int lr = ms.lens[r];
+                rank += (lr > lt || (lr == lt && r < tid)) ? 1 : 0;
+            }
+            if (rank == (int)blockIdx.z) ms.req = tid;
+        }
+        __syncthreads();
+        b = ms.req;
+    }
 
     // The query rows' loads go out first, ahead of the index loads and the
     // gathers that would otherwise queue in front of them (warps 8-15).
@@ -1034,6 +1058,7 @@ cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, cons
                            const mla_plan_t& plan, cudaStream_t stream)
 {
     constexpr int smem = smem_bytes<N, SPARSE>();
+    static_assert(smem <= 227 * 1024, "one CTA's dynamic shared memory limit");
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {

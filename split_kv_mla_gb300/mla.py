@@ -47,7 +47,8 @@ class mla_plan_t(ctypes.Structure):
         ("batch", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_heads", ctypes.c_int32),
         ("d_v", ctypes.c_int32), ("d_rope", ctypes.c_int32), ("sm_count", ctypes.c_int32),
         ("total_keys", ctypes.c_int64), ("kv_share", ctypes.c_int32),
-        ("extra_topk", ctypes.c_int32),
+        ("extra_topk", ctypes.c_int32), ("long_first", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -196,3 +196,19 @@ def test_decode_rejects_inconsistent_kv_share(lib):
         q.kv_share = share
         heads = q.num_heads
         assert _call_decode(lib, q, ws_bytes=q.workspace_bytes, heads=heads) == -1, share
+
+
+@pytest.mark.parametrize("tokens,splits", [(1, 16), (8, 8), (24, 2), (64, 1)])
+def test_sparse_plan_matches_the_measured_best_split(tokens, splits):
+    # 64 heads, top-k 2048, 152 SMs: the split counts a forced-split sweep of the
+    # sparse workload measured fastest on GB300 (the c4 token counts)
+    assert mla.mla_sparse_decode_plan(tokens, 64, 2048, 152).num_splits == splits
+
+
+def test_long_first_only_when_the_grid_outlasts_a_wave():
+    # B=64 H=128 (256 CTAs > one wave): longest requests first; c1 (128 CTAs): not
+    assert mla.mla_decode_plan(64, 1, 128, 64 * 16896, 152).long_first == 1
+    assert mla.mla_decode_plan(8, 1, 16, 8 * 8192, 152).long_first == 0
+    assert mla.mla_decode_plan(1, 1, 64, 131072, 152).long_first == 0
+    assert mla.mla_decode_plan(300, 1, 128, 300 * 4096, 152).long_first == 0   # batch > 256
+    assert mla.mla_sparse_decode_plan(64, 64, 2048, 152).long_first == 0

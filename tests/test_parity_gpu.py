@@ -135,6 +135,23 @@ def test_deterministic_run_to_run():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_long_first_ordering_is_bit_exact():
+    # variable lengths over more CTAs than one wave: serving the longest
+    # requests first must not change a single bit
+    lens = gen.variable_lengths(48, 16, 3000, seed=8)
+    inp = gen.dense_inputs(48, 1, 128, lens, seed=8)
+    plan = mla.mla_decode_plan(inp.batch, 1, 128, inp.total_keys, mla.sm_count())
+    assert plan.long_first == 1
+    o1, l1, _ = run_dense(inp, plan=plan)
+    plan.long_first = 0
+    o2, l2, _ = run_dense(inp, plan=plan)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    sel = sample_items(48 * 128, 64, seed=2)
+    ro, rl = oracle.dense_decode(inp, sel)
+    compare(o1.reshape(-1, 512)[torch.as_tensor(sel)], l1.reshape(-1)[torch.as_tensor(sel)],
+            ro, rl, "long first")
+
+
 def test_page_table_permutation_is_bit_exact():
     inp = gen.dense_inputs(3, 2, 16, [900, 1300, 77], seed=12, extra_slots=40)
     o1, l1, _ = run_dense(inp)

@@ -439,40 +439,74 @@ def e2e_measure(runner, stream, steps):
     that step's queries and page table from pinned host memory to the device
     (one copy of a packed buffer), runs the decode, and copies o and lse back
     (one copy of a packed buffer); the KV pool is resident cache state and
-    rotates over the device copies like the main arm.  The steps are replayed
-    from a CUDA graph, as a serving loop would."""
+    rotates over the device copies like the main arm.  As a serving loop would,
+    the steps are replayed from a CUDA graph and pipelined over two sets of
+    buffers: step i's input copy (one copy stream) and step i-1's result copy
+    (another) overlap the decode of the step in between, and a buffer is reused
+    only after the step two back has finished with it."""
     inp = runner.inp
     names = runner.input_names()
     src = [getattr(inp, n).contiguous() for n in names]
     host_in, host_views = _packed(src, pinned=True)
     for hv, t in zip(host_views, src):
         hv.copy_(t)
-    dev_in, dv = _packed(src, device=runner.device)
-    d = dict(zip(names, dv))
-    dev_out, (o, lse) = _packed([runner.o, runner.lse], device=runner.device)
-    host_out, _ = _packed([runner.o, runner.lse], pinned=True)
+    dev_in, dviews, dev_out, outs, host_out = [], [], [], [], []
+    for _ in range(2):
+        buf, views = _packed(src, device=runner.device)
+        dev_in.append(buf)
+        dviews.append(dict(zip(names, views)))
+        obuf, (o, lse) = _packed([runner.o, runner.lse], device=runner.device)
+        dev_out.append(obuf)
+        outs.append((o, lse))
+        host_out.append(_packed([runner.o, runner.lse], pinned=True)[0])
     h2d = host_in.numel()
-    d2h = host_out.numel()
+    d2h = host_out[0].numel()
     plan = runner.plan
     copies = runner.copies
+    c_in = torch.cuda.Stream(runner.device)
+    c_out = torch.cuda.Stream(runner.device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def one(i):
-        dev_in.copy_(host_in, non_blocking=True)
+    def one(i, first):
+        k = i % 2
+        d = dviews[k]
+        o, lse = outs[k]
+        with torch.cuda.stream(c_in):
+            if not first:
+                c_in.wait_event(ev_done[k])      # step i-2 has read dev_in[k]
+            dev_in[k].copy_(host_in, non_blocking=True)
+            ev_in[k].record(c_in)
+        stream.wait_event(ev_in[k])
+        if not first:
+            stream.wait_event(ev_out[k])         # step i-2's result has left dev_out[k]
         if "extra_pool" in copies[0]:
             d["extra_pool"] = copies[i % len(copies)]["extra_pool"]
         runner.call(d, copies[i % len(copies)]["pool"], o, lse, stream, plan=plan)
-        host_out.copy_(dev_out, non_blocking=True)
+        ev_done[k].record(stream)
+        with torch.cuda.stream(c_out):
+            c_out.wait_event(ev_done[k])
+            host_out[k].copy_(dev_out[k], non_blocking=True)
+            ev_out[k].record(c_out)
 
-    n = len(copies)
+    def run(n):
+        # the copy streams fork from and join back into the decode stream
+        c_in.wait_stream(stream)
+        c_out.wait_stream(stream)
+        for i in range(n):
+            one(i, i < 2)
+        stream.wait_stream(c_in)
+        stream.wait_stream(c_out)
+
+    n = max(2, len(copies))
     with torch.cuda.stream(stream):
-        for i in range(3):
-            one(i)
+        run(3)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                one(i)
+            run(n)
     reps = max(1, steps // n)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)

@@ -126,6 +126,12 @@ __device__ __forceinline__ void tc_fence_after()
 
 // ---- TMA ---------------------------------------------------------------------------------------
 
+// Bring the 128-byte line holding p into L2 (a hint; no data returned).
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -84,6 +84,7 @@ static_assert(kTau + kShift < 8.807f, "p * 2^kShift stays below e4m3's largest f
 constexpr int kQWarps = kWarps - kSoftmaxWarp0;   // warps 8-15 split the query tile
 constexpr uint32_t kQBar = 2;                     // Q tile + MMA warp (1 and 3: softmax sets)
 constexpr uint32_t kGatherSleepNs = 32;
+constexpr int kPrefetchMaxBlocks = 8;             // unshared CTAs prefetch up to this many blocks
 constexpr uint32_t kMmaSleepNs = 32;
 
 template <int N, bool SPARSE>
@@ -515,6 +516,24 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 tma_gather4(dst, map, x, sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
         }
     };
+    // L2 prefetch of the rows of block j ahead of their gather (row tid, split
+    // over the cluster's ranks): one prefetch per 128-byte line, from indices
+    // loaded a block earlier so it never waits on a load.  Measured on GB300 it
+    // pays with KV sharing (B=8 H=64 S=131072: 284.7 -> 275.3 us) and for CTAs
+    // of a few blocks (B=8 H=16 S=8192: 19.1 -> 18.7 us) but slows long
+    // unshared streams (B=8 H=16 S=131072: 139 -> 178 us), so it is off there.
+    const bool prefetch = CH > 1 || nblk <= kPrefetchMaxBlocks;
+    auto prefetch_block = [&](int j, int32_t v) {
+        const int kb = k0 + j * kBlockN;
+        const int nk = min(kBlockN, k1 - kb);
+        if (!prefetch || !row_lane || tid >= nk || (tid % CH) != rank) return;
+        const bool ex = key_extra(kb + tid);
+        if (!slot_ok(v, ex)) return;
+        const uint8_t* row = (ex ? a.extra_pool : a.pool) + (int64_t)v * kWidth;
+#pragma unroll
+        for (int c = 0; c < kWidth; c += 128) prefetch_l2(row + c);
+    };
+    int32_t rpf = -1;   // row tid's index in the block after the next, for the prefetch
     Slots gnext{};
     int32_t rnext = -1;
     Slots s0{{-1, -1, -1, -1}, false}, s1{{-1, -1, -1, -1}, false};
@@ -535,6 +554,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             gnext = raw_slots(2);
             rnext = raw_row(2);
         }
+        if (prefetch && nblk > 3) rpf = raw_row(3);
     }
 
     // ---- barriers and TMEM ----------------------------------------------------------------
@@ -551,6 +571,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         // start the first two blocks before anything else
         issue(0, fix_slots(s0), row_valid(0, w0));
         if (nblk > 1) issue(1, fix_slots(s1), row_valid(1, w1));
+        if (nblk > 2) prefetch_block(2, rnext);
     }
 
     // ---- the query tile: one warp per row, warps 8-15 --------------------------------------------
@@ -626,6 +647,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             if (j + 1 < nblk) {
                 gnext = raw_slots(j + 1);
                 rnext = raw_row(j + 1);
+                prefetch_block(j + 1, rpf);   // block j + 1's rows into L2
+                if (prefetch && j + 2 < nblk) rpf = raw_row(j + 2);
             }
         }
         // Never leave the CTA with loads in flight: the last two issued blocks

@@ -46,6 +46,12 @@
 //   running sum.  The sums of p_hi + p_lo (what the tensor core consumed, used
 //   to normalise O) are kept per thread and row across blocks (the split into
 //   e4m3 terms yields them) and reduced once, at the end.
+// * Memory in flight.  Two stages hold gathered blocks; right after issuing
+//   block j, warps 0-3 prefetch the rows of block j+1 into L2 so its gather
+//   finds them there (with KV sharing, or in CTAs of a few blocks, where
+//   measurement showed a gain).
+// * Work order.  When the grid outlasts one wave, grid slice z serves the z-th
+//   longest request, so variable-length batches start their longest work first.
 // * Safety.  Every mbarrier wait is time-bounded and warp-uniform; the softmax
 //   warps meet at bar.sync only at points every one of them reaches, and agree
 //   on giving up through the same barrier-reduction, so a stuck pipeline ends

@@ -47,9 +47,8 @@
 //   to normalise O) are kept per thread and row across blocks (the split into
 //   e4m3 terms yields them) and reduced once, at the end.
 // * Memory in flight.  Two stages hold gathered blocks; right after issuing
-//   block j, warps 0-3 prefetch the rows of block j+1 into L2 so its gather
-//   finds them there (with KV sharing, or in CTAs of a few blocks, where
-//   measurement showed a gain).
+//   block j, the gather warps prefetch the rows of block j+1 into L2 so its
+//   gather finds them there.
 // * Work order.  When the grid outlasts one wave, grid slice z serves the z-th
 //   longest request, so variable-length batches start their longest work first.
 // * Safety.  Every mbarrier wait is time-bounded and warp-uniform; the softmax
@@ -90,7 +89,7 @@ static_assert(kTau + kShift < 8.807f, "p * 2^kShift stays below e4m3's largest f
 constexpr int kQWarps = kWarps - kSoftmaxWarp0;   // warps 8-15 split the query tile
 constexpr uint32_t kQBar = 2;                     // Q tile + MMA warp (1 and 3: softmax sets)
 constexpr uint32_t kGatherSleepNs = 32;
-constexpr int kPrefetchMaxBlocks = 8;             // unshared CTAs prefetch up to this many blocks
+constexpr int kPrefetchMaxBlocks = 8;             // unshared CTAs of more blocks prefetch by line
 constexpr uint32_t kMmaSleepNs = 32;
 
 template <int N, bool SPARSE>
@@ -522,24 +521,59 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 tma_gather4(dst, map, x, sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
         }
     };
-    // L2 prefetch of the rows of block j ahead of their gather (row tid, split
-    // over the cluster's ranks): one prefetch per 128-byte line, from indices
-    // loaded a block earlier so it never waits on a load.  Measured on GB300 it
-    // pays with KV sharing (B=8 H=64 S=131072: 284.7 -> 275.3 us) and for CTAs
-    // of a few blocks (B=8 H=16 S=8192: 19.1 -> 18.7 us) but slows long
-    // unshared streams (B=8 H=16 S=131072: 139 -> 178 us), so it is off there.
-    const bool prefetch = CH > 1 || nblk <= kPrefetchMaxBlocks;
+    // L2 prefetch of the rows of block j+1 right after issuing block j, one
+    // prefetch per 128-byte line, from indices loaded a block earlier so it
+    // never waits on a load; the next gather then finds its rows in L2.  Two
+    // ways to deal the lines out, each where it measured best on GB300:
+    //  * by row: warps 0-3, thread tid prefetching row tid (rows split over the
+    //    cluster's ranks) -- with KV sharing (B=8 H=64 S=131072: 284.7 ->
+    //    275.3 us) and in CTAs of a few blocks (B=8 H=16 S=8192: 19.1 -> 18.7);
+    //  * by line, over all seven gather warps -- in long unshared streams,
+    //    where prefetching by row held up warps 0-3, which also issue gathers
+    //    (B=8 H=16 S=131072: 139 us without a prefetch, 178 by row, 135 by line).
+    const bool pf_rows = CH > 1 || nblk <= kPrefetchMaxBlocks;
     auto prefetch_block = [&](int j, int32_t v) {
         const int kb = k0 + j * kBlockN;
         const int nk = min(kBlockN, k1 - kb);
-        if (!prefetch || !row_lane || tid >= nk || (tid % CH) != rank) return;
+        if (!pf_rows || !row_lane || tid >= nk || (tid % CH) != rank) return;
         const bool ex = key_extra(kb + tid);
         if (!slot_ok(v, ex)) return;
         const uint8_t* row = (ex ? a.extra_pool : a.pool) + (int64_t)v * kWidth;
 #pragma unroll
         for (int c = 0; c < kWidth; c += 128) prefetch_l2(row + c);
     };
-    int32_t rpf = -1;   // row tid's index in the block after the next, for the prefetch
+    constexpr int kLines = (kWidth + 127) / 128;                 // 128-byte lines per row
+    constexpr int kPfPer = (kBlockN * kLines + kGatherWarps * 32 - 1) / (kGatherWarps * 32);
+    struct PfLines { int32_t v[kPfPer]; };   // slots of this thread's lines (-1: none)
+    auto pf_lines_load = [&](int j) -> PfLines {
+        PfLines r;
+        const int kb = k0 + j * kBlockN;
+        const int nk = min(kBlockN, k1 - kb);
+#pragma unroll
+        for (int i = 0; i < kPfPer; ++i) {
+            const int item = tid + kGatherWarps * 32 * i;
+            const int row = item / kLines;
+            r.v[i] = (!pf_rows && item < kBlockN * kLines && row < nk) ? key_slot(kb + row) : -1;
+        }
+        return r;
+    };
+    auto pf_lines_issue = [&](int j, const PfLines& r) {
+        const int kb = k0 + j * kBlockN;
+#pragma unroll
+        for (int i = 0; i < kPfPer; ++i) {
+            const int item = tid + kGatherWarps * 32 * i;
+            const int row = item / kLines;
+            if (r.v[i] < 0) continue;
+            const bool ex = key_extra(kb + row);
+            if (!slot_ok(r.v[i], ex)) continue;
+            prefetch_l2((ex ? a.extra_pool : a.pool) + (int64_t)r.v[i] * kWidth +
+                        (item % kLines) * 128);
+        }
+    };
+    int32_t rpf = -1;   // by row: row tid's index in the block after the next
+    PfLines lpf2, lpf;   // by line: block 2's lines, then the block after the next
+#pragma unroll
+    for (int i = 0; i < kPfPer; ++i) lpf2.v[i] = lpf.v[i] = -1;
     Slots gnext{};
     int32_t rnext = -1;
     Slots s0{{-1, -1, -1, -1}, false}, s1{{-1, -1, -1, -1}, false};
@@ -560,7 +594,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             gnext = raw_slots(2);
             rnext = raw_row(2);
         }
-        if (prefetch && nblk > 3) rpf = raw_row(3);
+        if (pf_rows && nblk > 3) rpf = raw_row(3);
+        if (!pf_rows && nblk > 2) lpf2 = pf_lines_load(2);
+        if (!pf_rows && nblk > 3) lpf = pf_lines_load(3);
     }
 
     // ---- barriers and TMEM ----------------------------------------------------------------
@@ -577,7 +613,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         // start the first two blocks before anything else
         issue(0, fix_slots(s0), row_valid(0, w0));
         if (nblk > 1) issue(1, fix_slots(s1), row_valid(1, w1));
-        if (nblk > 2) prefetch_block(2, rnext);
+        if (nblk > 2) {
+            prefetch_block(2, rnext);
+            pf_lines_issue(2, lpf2);
+        }
     }
 
     // ---- the query tile: one warp per row, warps 8-15 --------------------------------------------
@@ -654,7 +693,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 gnext = raw_slots(j + 1);
                 rnext = raw_row(j + 1);
                 prefetch_block(j + 1, rpf);   // block j + 1's rows into L2
-                if (prefetch && j + 2 < nblk) rpf = raw_row(j + 2);
+                pf_lines_issue(j + 1, lpf);
+                if (pf_rows && j + 2 < nblk) rpf = raw_row(j + 2);
+                if (!pf_rows && j + 2 < nblk) lpf = pf_lines_load(j + 2);
             }
         }
         // Never leave the CTA with loads in flight: the last two issued blocks

@@ -12,12 +12,16 @@ from .mla import (  # noqa: F401
     mla_dcp_lse_merge_ranks,
     mla_decode,
     mla_decode_dcp,
+    mla_decode_dcp_splits,
+    mla_decode_noalloc,
     mla_decode_splits,
     mla_decode_plan,
     mla_plan_force_splits,
     mla_plan_t,
     mla_read_device_error,
     mla_sparse_decode,
+    mla_sparse_decode_extra,
+    mla_sparse_decode_extra_splits,
     mla_sparse_decode_splits,
     mla_sparse_decode_plan,
     mla_splitk_reduce,

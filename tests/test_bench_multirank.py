@@ -71,3 +71,31 @@ def test_pages_baseline_only_for_the_pages_own_shapes():
     assert bench.pages_baseline_gbs("p-16-150000") == pytest.approx(1700.0)
     assert bench.pages_baseline_gbs("c1q1") is None
     assert bench.pages_baseline_gbs("c3") is None
+
+
+@pytest.mark.parametrize("name,kind", [
+    ("c0", "dense"), ("c1q1", "dense"), ("c1q4", "dense"), ("c2-2x4096", "dense"),
+    ("c4-1", "sparse"), ("c4x-1", "sparse"), ("d-2-16-3-100", "dense"),
+    ("p-2-256", "dense"), ("dcp2-c0", "dcp"),
+])
+def test_every_workload_name_parses(name, kind):
+    sys.path.insert(0, ROOT)
+    import bench
+    k, inp, desc = bench.make_workload(name)
+    assert k == kind and desc
+    assert bench.kv_bytes_per_call(k, inp) == bench.keys_per_call(k, inp) * bench.row_bytes(k)
+
+
+def test_packed_buffers_are_256_byte_aligned_views():
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch
+    ts = [torch.arange(5, dtype=torch.int32), torch.ones(3, 7, dtype=torch.bfloat16),
+          torch.zeros(1, dtype=torch.float32)]
+    buf, views = bench._packed(ts)
+    for v, t in zip(views, ts):
+        assert v.shape == t.shape and v.dtype == t.dtype
+        assert (v.data_ptr() - buf.data_ptr()) % 256 == 0
+        v.copy_(t)
+    for v, t in zip(views, ts):
+        assert torch.equal(v, t)

@@ -586,6 +586,87 @@ def _oracle_items(kind, inp, items):
         oracle.sparse_decode(inp, sel)
 
 
+# Every synthetic workload timed next to the headline one in the same run (the
+# five configurations of the benchmark: c0, c1 at q_len 1 and 4, the four
+# split-heavy c2 points, the variable-length c3 batch and the sparse c4 token
+# counts).
+ALL_WORKLOADS = ["c0", "c1q1", "c1q4", "c2-1x131072", "c2-2x65536", "c2-8x131072",
+                 "c2-16x131072", "c3", "c4-1", "c4-8", "c4-24", "c4-64"]
+
+
+def bf16_peak_tflops():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def l2_copies(kind, inp, l2):
+    """(copies, bytes per copy): device copies of the inputs whose rotation
+    exceeds 4x L2, so every call streams its KV from HBM."""
+    dense = kind != "sparse"
+    per_copy = (inp.pool.numel() + (inp.q_lat.numel() * 2 if dense else inp.q_nope.numel() * 2)
+                + inp.q_pe.numel() * 2 + (inp.kv_indices.numel() * 4 if dense
+                                          else inp.indices.numel() * 4))
+    if not dense and inp.extra_topk:
+        per_copy += inp.extra_pool.numel() + inp.extra_indices.numel() * 4
+    return max(1, min(64, math.ceil(4 * l2 / max(per_copy, 1)))), per_copy
+
+
+def measure_workload(name, device, world, steps, cpu_budget):
+    """One workload's call time (graph replays over rotating inputs), its split
+    kernel's own time, and the oracle on the host for a short sample."""
+    kind, inp, desc = make_workload(name)
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
+    copies, _ = l2_copies(kind, inp, l2)
+    runner = Runner(kind, inp, device, copies)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            runner.step(i, stream)
+    torch.cuda.synchronize()
+    g_full, g_rem, full, start, end = time_steps(runner, stream, steps, copies)
+    with torch.cuda.stream(stream):
+        if g_full is not None:
+            g_full.replay()
+        start.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end) / steps, world, device)
+    split_ms, _ = kernel_times(runner, stream, steps, ms)
+    split_ms = max_over_ranks(split_ms, world, device)
+    peak, _ = measured_peaks()
+    tpeak, _ = bf16_peak_tflops()
+    kv = kv_bytes_per_call(kind, inp)
+    flops = flops_per_call(kind, inp)
+    gbs = kv / (ms * 1e-3) / 1e9
+    out = {"desc": desc, "us_per_call": round(ms * 1e3, 3),
+           "kv_gbs": round(gbs * world, 2),
+           "keys_per_s": keys_per_call(kind, inp) * world / (ms * 1e-3),
+           "frac_of_measured_hbm": round(gbs / peak, 4),
+           "split_kernel_us": round(split_ms * 1e3, 3),
+           "split_kernel_frac_of_measured_hbm": round(kv / (split_ms * 1e-3) / 1e9 / peak, 4),
+           "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+           "frac_of_bf16_tensor_peak": round(flops / (ms * 1e-3) / 1e12 / tpeak, 4),
+           "flop_per_kv_byte": round(flops / kv, 1),
+           "bound": "tensor" if flops / kv > tpeak * 1e12 / (peak * 1e9) else "hbm",
+           "num_splits": runner.plan.num_splits, "head_blocks": runner.plan.head_blocks}
+    if cpu_budget > 0:
+        cb = cpu_baseline(kind, inp, cpu_budget)
+        out["oracle_gbs"] = round(cb["value"], 4)
+        out["oracle_sample"] = cb["sample"]
+    del runner, g_full, g_rem
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
@@ -595,14 +676,8 @@ def run_ours(args, rank, world, local_rank):
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     # rotation copies: total input bytes > 4x L2
-    from split_kv_mla_gb300 import mla as _m  # noqa: F401
     dense = kind != "sparse"
-    per_copy = (inp.pool.numel() + (inp.q_lat.numel() * 2 if dense else inp.q_nope.numel() * 2)
-                + inp.q_pe.numel() * 2 + (inp.kv_indices.numel() * 4 if dense
-                                          else inp.indices.numel() * 4))
-    if not dense and inp.extra_topk:
-        per_copy += inp.extra_pool.numel() + inp.extra_indices.numel() * 4
-    copies = max(1, min(64, math.ceil(4 * l2 / max(per_copy, 1))))
+    copies, per_copy = l2_copies(kind, inp, l2)
     runner = (DcpRunner(inp, device, copies, args.splits) if kind == "dcp"
               else Runner(kind, inp, device, copies, args.splits))
     stream = torch.cuda.Stream(device)
@@ -662,8 +737,6 @@ def run_ours(args, rank, world, local_rank):
     achieved = bytes_call / (split_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
 
-    if rank != 0:
-        return None
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -699,8 +772,21 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "tflops": flops_per_call(kind, inp) / (ms_step * 1e-3) / 1e12,
     }
-    if not args.no_cpu_baseline:
+    # the oracle baseline runs on rank 0 of a single-GPU run only
+    oracle_here = not args.no_cpu_baseline and rank == 0 and world == 1
+    if oracle_here:
         out["cpu_baseline"] = cpu_baseline(kind, inp, args.cpu_budget)
+    if args.workloads != "none":
+        names = ALL_WORKLOADS if args.workloads == "all" else args.workloads.split(",")
+        del runner
+        torch.cuda.empty_cache()
+        sweep = {}
+        for name in names:
+            sweep[name] = measure_workload(
+                name, device, world, args.workload_steps,
+                args.workload_cpu_budget if oracle_here else 0.0)
+        if rank == 0:
+            out["workloads"] = sweep
     return out
 
 
@@ -747,9 +833,35 @@ def run_reference(args, rank, world):
     }
 
 
-def main():
+def _free_port() -> int:
+    import socket
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    return port
+
+
+def _rank_entry(rank, world, port, argv, target):
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    target(argv)
+
+
+def spawn_ranks(world: int, argv, target=None) -> None:
+    """Run `target(argv)` (default: this benchmark) in `world` fresh processes,
+    one rank per GPU of this node, as torchrun would: RANK, LOCAL_RANK,
+    WORLD_SIZE and a 127.0.0.1 rendezvous in the environment."""
+    import torch.multiprocessing as mp
+    mp.start_processes(_rank_entry, args=(world, _free_port(), list(argv), target or main),
+                       nprocs=world, join=True, start_method="spawn")
+
+
+def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="ranks (one per GPU); without torchrun, spawns that many processes")
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -759,10 +871,18 @@ def main():
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--splits", type=int, default=0,
                     help="force the split count instead of the planner's (split sweeps)")
-    args = ap.parse_args()
+    ap.add_argument("--workloads", default="all",
+                    help="also time these workloads in the same run: all, none, or a "
+                         "comma-separated list")
+    ap.add_argument("--workload-steps", type=int, default=200)
+    ap.add_argument("--workload-cpu-budget", type=float, default=1.5)
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        spawn_ranks(args.gpus, sys.argv[1:] if argv is None else argv)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -775,7 +895,7 @@ def main():
         out = run_ours(args, rank, world, local_rank)
         if world > 1:
             torch.distributed.destroy_process_group()
-    if out is not None:
+    if out is not None and rank == 0:
         print(json.dumps(out), flush=True)
 
 

@@ -26,7 +26,6 @@ inline int32_t rows_per_cta_for(int64_t rows) { return rows <= 16 ? 16 : 32; }
 // (blocks per CTA x block time + per-CTA fixed time), plus the reduce (a launch
 // and the fp32 partial traffic) when there is more than one split.
 constexpr double kBlockUs = 1.65;      // 128 x 576 B at one SM's share of HBM bandwidth
-constexpr double kComputeUs = 0.9;     // QK, softmax and PV of one block (floor with a shared gather)
 constexpr double kCtaUs = 2.0;         // prologue, pipeline fill, epilogue
 constexpr double kReduceUs = 2.0;      // reduce launch and its latency chain
 constexpr double kBytesPerUs = 6.8e6;  // HBM bytes per microsecond
@@ -34,23 +33,8 @@ constexpr double kBytesPerUs = 6.8e6;  // HBM bytes per microsecond
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
-// Head blocks that share each gathered KV block (a cluster with TMA multicast):
-// the largest of 4 and 2 dividing head_blocks when a CTA holds 32 rows.
-int32_t kv_share_for(int32_t rows_per_cta, int64_t head_blocks)
-{
-    if (rows_per_cta != 32) return 1;
-    if (head_blocks % 4 == 0) return 4;
-    if (head_blocks % 2 == 0) return 2;
-    return 1;
-}
-
-// CTAs resident at once in clusters of `share` at one CTA per SM (GB300:
-// clusters of 4 leave 8 of the 152 SMs idle, measured with
-// cudaOccupancyMaxActiveClusters).
-int64_t wave_ctas(int32_t share, int32_t sm_count)
-{
-    return share >= 4 ? (int64_t)sm_count - sm_count / 19 : sm_count;
-}
+// CTAs resident at once: one per SM.
+int64_t wave_ctas(int32_t sm_count) { return sm_count; }
 
 int device_ok()
 {
@@ -81,16 +65,14 @@ int64_t workspace_for(int64_t items, int ns, int d_v)
 }
 
 // Split count for `tiles` (request, head block) tiles, `keys` keys per
-// request, `items` output rows (row x head) in the call and a KV block shared
-// by `share` CTAs.
-int32_t gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v, int32_t sm_count,
-                     int32_t share)
+// request and `items` output rows (row x head) in the call.
+int32_t gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v, int32_t sm_count)
 {
     const int64_t blocks = ceil_div(keys > 0 ? keys : 1, kBlockN);
     const int64_t ctas = tiles > 0 ? tiles : 1;
     const int64_t max_ns = blocks < MLA_MAX_SPLITS ? blocks : MLA_MAX_SPLITS;
-    const double block_us = kBlockUs / share > kComputeUs ? kBlockUs / share : kComputeUs;
-    const int64_t wave = wave_ctas(share, sm_count);
+    const double block_us = kBlockUs;
+    const int64_t wave = wave_ctas(sm_count);
     double best = 0.0;
     int32_t best_ns = 1;
     for (int64_t ns = 1; ns <= max_ns; ++ns) {
@@ -131,7 +113,7 @@ int32_t sparse_splits(int64_t ctas, int64_t topk, int32_t sm_count)
 }
 
 void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32_t d_v,
-               int32_t d_rope, int32_t sm_count, int64_t total_keys, int32_t ns, int32_t share)
+               int32_t d_rope, int32_t sm_count, int64_t total_keys, int32_t ns)
 {
     const int32_t rows = q_len * heads;
     std::memset(p, 0, sizeof *p);
@@ -151,13 +133,26 @@ void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32
     p->d_rope = d_rope;
     p->sm_count = sm_count;
     p->total_keys = total_keys;
-    p->kv_share = share;
+    p->kv_share = 1;
 }
+
+}  // namespace
+
+// The workspace bytes a plan needs, from its shape and split count (the plan's
+// own workspace_bytes field is only a copy of this, and is checked against it).
+int64_t needed_workspace(const mla_plan_t* plan)
+{
+    return workspace_for((int64_t)plan->batch * plan->q_len * plan->num_heads,
+                         plan->num_splits, plan->d_v);
+}
+
+namespace {
 
 int check_workspace(const mla_plan_t* plan, const void* ws, int64_t bytes)
 {
     if (!ws) return MLA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MLA_ERR_MISALIGNED;
+    if (plan->workspace_bytes != needed_workspace(plan)) return MLA_ERR_INVALID_ARG;
     if (bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
     return MLA_OK;
 }
@@ -176,15 +171,22 @@ void carve(const mla_plan_t* plan, void* ws, int64_t items, SplitArgs* a)
     }
 }
 
+// A plan's launch geometry must be the one the planner derives from its shape
+// and split count: the kernels index the workspace and the outputs by it.
 bool variant_ok(const mla_plan_t* plan)
 {
     if (plan->variant != kVariantTc) return false;
+    if (plan->q_len < 1 || plan->num_heads < 1 || plan->batch < 0) return false;
+    const int64_t rows = (int64_t)plan->q_len * plan->num_heads;
+    if (rows > (1 << 20)) return false;
+    if (plan->rows_per_cta != rows_per_cta_for(rows) || plan->block_n != kBlockN ||
+        plan->head_blocks != ceil_div(rows, plan->rows_per_cta) ||
+        plan->grid_x != plan->head_blocks || plan->grid_y != plan->num_splits ||
+        plan->grid_z != plan->batch)
+        return false;
     if (plan->long_first != 0 && (plan->long_first != 1 || plan->batch > kLongFirstMaxBatch))
         return false;
-    const int32_t sh = plan->kv_share;
-    if (sh != 1 && sh != 2 && sh != 4) return false;
-    if (sh > 1 && (plan->rows_per_cta != 32 || plan->head_blocks % sh != 0)) return false;
-    return true;
+    return plan->kv_share == 1;
 }
 
 int run(const mla_plan_t* plan, SplitArgs& a, int64_t items, cudaStream_t stream,
@@ -248,15 +250,14 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
     if (rows > (1 << 20)) return MLA_ERR_UNSUPPORTED_SHAPE;
     const int64_t head_blocks = ceil_div(rows, rows_per_cta_for(rows));
     const int64_t keys = batch > 0 ? ceil_div(total_keys, batch) : 0;
-    const int32_t share = kv_share_for(rows_per_cta_for(rows), head_blocks);
     const int32_t ns = gb300_splits(head_blocks * (batch > 0 ? batch : 1), keys,
-                                    (int64_t)batch * rows, d_v, sm_count, share);
-    fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ns, share);
+                                    (int64_t)batch * rows, d_v, sm_count);
+    fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ns);
     // Longest requests first once the grid outlasts one wave (variable lengths
     // then leave the short requests for the last wave).
     const int64_t ctas = (int64_t)out->grid_x * out->grid_y * out->grid_z;
     out->long_first = (batch >= 2 && batch <= kLongFirstMaxBatch &&
-                       ctas > wave_ctas(share, sm_count)) ? 1 : 0;
+                       ctas > wave_ctas(sm_count)) ? 1 : 0;
     return MLA_OK;
 }
 
@@ -276,8 +277,7 @@ int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
                                (int64_t)topk + extra_topk, sm_count);
     if (ns > cap) ns = cap;
     fill_plan(out, num_tokens, 1, num_heads, d_v, d_rope, sm_count,
-              (int64_t)num_tokens * ((int64_t)topk + extra_topk), ns,
-              kv_share_for(rows_per_cta_for(num_heads), head_blocks));
+              (int64_t)num_tokens * ((int64_t)topk + extra_topk), ns);
     out->extra_topk = extra_topk;
     return MLA_OK;
 }

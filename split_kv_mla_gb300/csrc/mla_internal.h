@@ -1,12 +1,40 @@
 // mla_internal.h -- host-side declarations shared by the libmla translation units.
 #pragma once
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/mla_decode.h"
 
 namespace mla {
+
+// Runs a set-up step (a kernel attribute, a symbol lookup: state the runtime
+// keeps per device) once for each device that is current when run() is called.
+// Thread-safe; a step that fails is tried again on the next call.
+class DeviceOnce {
+public:
+    template <class F>
+    cudaError_t run(F&& step)
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+        e = step();
+        if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+        return e;
+    }
+
+private:
+    static constexpr int kMaxDevices = 64;
+    std::atomic<bool> done_[kMaxDevices]{};
+    std::mutex mu_;
+};
 
 // Parameters of one split-kernel launch (dense or sparse).
 // Largest batch for which the split kernel orders requests longest first.
@@ -58,6 +86,9 @@ enum Variant : int32_t {
 };
 
 cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream);
+
+// Workspace bytes that a plan needs, recomputed from its shape and split count.
+int64_t needed_workspace(const mla_plan_t* plan);
 
 // 2-D uint8 tensor map of the pool (row_bytes columns x rows) with one-row
 // boxes of `box` columns (the shape tile::gather4 reads); false on failure.

@@ -50,7 +50,10 @@ extern "C" int mla_decode_noalloc(const mla_plan_t* plan, const void* q_lat, con
                                   float kv_scale, void* o_lat, float* lse, void* stream)
 {
     if (!plan) return MLA_ERR_INVALID_ARG;
-    if (plan->workspace_bytes > (int64_t)MLA_NOALLOC_SCRATCH_BYTES)
+    // The scratch need comes from the plan's shape and split count, not from
+    // its workspace_bytes field, which a caller could have edited; mla_decode
+    // rejects a plan whose field disagrees with that need.
+    if (mla::needed_workspace(plan) > (int64_t)MLA_NOALLOC_SCRATCH_BYTES)
         return MLA_ERR_WORKSPACE_TOO_SMALL;
     void* scratch = nullptr;
     int rc = scratch_for_current_device(&scratch);

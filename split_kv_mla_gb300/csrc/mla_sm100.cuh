@@ -150,21 +150,6 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
-// tma_gather4 delivered to the same shared-memory offset in every CTA of the
-// cluster named by cta_mask; each destination CTA's mbarrier at bar's offset
-// receives the bytes that land there.
-__device__ __forceinline__ void tma_gather4_multicast(void* dst, const void* tmap, int32_t x,
-                                                      int32_t r0, int32_t r1, int32_t r2,
-                                                      int32_t r3, uint64_t* bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(r0), "r"(r1),
-          "r"(r2), "r"(r3), "r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
-
 // ---- register reallocation between warpgroups ---------------------------------------------
 
 // Lower / raise this warpgroup's registers per thread (all four warps of the
@@ -375,18 +360,7 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
         : "memory");
 }
 
-// The same commit, arriving on the mbarrier at this offset in every CTA of the
-// cluster named by cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;"
-        ::"r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
-
-// The same three operations for a converged warp: every lane passes the same
+// The same two operations for a converged warp: every lane passes the same
 // (warp-uniform) operands and lane 0 alone issues the instruction, predicated
 // rather than branched to, so the operands can stay in uniform registers.  The
 // issuing lane is always lane 0, so commits track that lane's MMAs.
@@ -411,18 +385,6 @@ __device__ __forceinline__ void umma_commit_warp(uint64_t* bar)
         "setp.eq.u32 e, l, 0;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
         ::"r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_commit_multicast_warp(uint64_t* bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\t"
-        "mov.u32 l, %%laneid;\n\t"
-        "setp.eq.u32 e, l, 0;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;\n\t}"
-        ::"r"(smem_u32(bar)), "h"(cta_mask)
         : "memory");
 }
 

@@ -61,7 +61,6 @@
 #include <math_constants.h>
 
 #include <climits>
-#include <mutex>
 
 #include "mla_internal.h"
 #include "mla_layout.cuh"
@@ -278,7 +277,7 @@ __device__ __forceinline__ void load_rows(uint32_t taddr_hi, uint32_t taddr_lo, 
     }
 }
 
-template <int N, bool SPARSE, int CH, bool EXTRA>
+template <int N, bool SPARSE, bool EXTRA>
 __global__ void __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 const __grid_constant__ CUtensorMap tm_rope, const SplitArgs a)
@@ -299,16 +298,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     asm volatile("griddepcontrol.launch_dependents;");
     const int rows_in_req = a.q_len * a.num_heads;
 
-    // With CH > 1 the CH head blocks of one (request, split) form a cluster that
-    // shares every gathered block: rank r issues the r-th share of the block's
-    // copies and multicasts them to all CH CTAs, so each KV byte leaves memory
-    // once.  A stage is refilled only when every CTA of the cluster has finished
-    // its P.V on it (kv_empty collects one arrival per CTA); pv_done is the
-    // CTA's own P.V completion.
+    // kv_empty: the stage's P.V has finished and it may be refilled; pv_done:
+    // the same completion, waited for by the softmax warps.
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.kv_full[i], kGatherWarps);   // one arrival per gather warp
-            mbar_init(&ms.kv_empty[i], CH);
+            mbar_init(&ms.kv_empty[i], 1);
             mbar_init(&ms.pv_done[i], 1);
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.s_free[i], 4 * kSets);   // every softmax warp
@@ -419,22 +414,16 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const int k1 = min(L, k0 + chunk);
     const int nblk = (k1 - k0 + kBlockN - 1) / kBlockN;
 
-    const int rank = CH > 1 ? (int)cluster_ctarank() : 0;
-    constexpr uint16_t kClusterMask = (uint16_t)((1u << CH) - 1u);
-
     // ---- gather helpers (warps 0-6) ---------------------------------------------------------
     // A block is 32 four-row groups x kBoxes boxes (the four 128-byte latent
-    // chunks, then the 64-byte RoPE chunk): kItems tile::gather4 copies, of
-    // which this CTA issues its cluster rank's share (all of them when CH == 1),
-    // dealt out kItemsPerWarp per warp and one per lane.  TMA issue is serial
-    // within a warp, so spreading the copies over seven warps shortens a
-    // block's issue.  The key-validity bits of all 128 rows are computed by every
-    // CTA itself (lanes of warps 0-3, one row each).
+    // chunks, then the 64-byte RoPE chunk): kItems tile::gather4 copies, dealt
+    // out kItemsPerWarp per warp and one per lane.  TMA issue is serial within a
+    // warp, so spreading the copies over seven warps shortens a block's issue.
+    // The key-validity bits of the 128 rows come from lanes of warps 0-3, one
+    // row each.
     constexpr int kBoxes = C::kRope ? 5 : 4;
     constexpr int kItems = 32 * kBoxes;
-    static_assert(kItems % CH == 0, "copies split evenly over the cluster");
-    constexpr int kItemsCta = kItems / CH;
-    constexpr int kItemsPerWarp = (kItemsCta + kGatherWarps - 1) / kGatherWarps;
+    constexpr int kItemsPerWarp = (kItems + kGatherWarps - 1) / kGatherWarps;
     static_assert(kItemsPerWarp <= 32, "one copy per lane");
     const int32_t* list = a.kv_indices + base;
     constexpr bool has_extra = EXTRA;   // only sparse launches have a second cache
@@ -446,9 +435,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         return k < topk4 ? -1 : __ldg(xlist + (k - topk4));
     };
     auto key_extra = [&](int k) { return has_extra && k >= topk4; };
-    const int cta_item = warp * kItemsPerWarp + lane;
-    const bool item_on = warp < kGatherWarps && lane < kItemsPerWarp && cta_item < kItemsCta;
-    const int my_item = rank * kItemsCta + cta_item;
+    const int my_item = warp * kItemsPerWarp + lane;
+    const bool item_on = warp < kGatherWarps && lane < kItemsPerWarp && my_item < kItems;
     const int my_group = item_on ? my_item / kBoxes : 0;   // rows 4 g .. 4 g + 3
     const int my_box = item_on ? my_item % kBoxes : 0;
     const bool row_lane = tid < kBlockN;                   // warps 0-3: row tid's validity
@@ -491,11 +479,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const int nk = min(kBlockN, k1 - kb);
         if (!row_lane || tid >= nk) return 0;
         if (slot_ok(v, key_extra(kb + tid))) return 1;
-        if (!(SPARSE && v < 0) && rank == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
+        if (!(SPARSE && v < 0)) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
         return 0;
     };
-    // Block j into stage j & 1 (of every CTA of the cluster).  Warp 0 announces
-    // the whole stage's bytes, which arrive from this CTA's and its peers' copies.
+    // Block j into stage j & 1.  Warp 0 announces the whole stage's bytes, which
+    // arrive from the seven warps' copies.
     auto issue = [&](int j, const Slots& sl, int rowok) {
         const int st = j & 1;
         if (row_lane) ms.kvalid[st][tid] = rowok;
@@ -514,28 +502,23 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             // sparse: tm_rope is the second cache's map (512-byte rows, no RoPE box)
             const CUtensorMap* map = (my_box < 4 && !sl.ex) ? &tm_lat : &tm_rope;
             const int x = my_box < 4 ? my_box * 128 : 512;
-            if (CH > 1)
-                tma_gather4_multicast(dst, map, x, sl.v[0], sl.v[1], sl.v[2], sl.v[3],
-                                      &ms.kv_full[st], kClusterMask);
-            else
-                tma_gather4(dst, map, x, sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
+            tma_gather4(dst, map, x, sl.v[0], sl.v[1], sl.v[2], sl.v[3], &ms.kv_full[st]);
         }
     };
     // L2 prefetch of the rows of block j+1 right after issuing block j, one
     // prefetch per 128-byte line, from indices loaded a block earlier so it
     // never waits on a load; the next gather then finds its rows in L2.  Two
     // ways to deal the lines out, each where it measured best on GB300:
-    //  * by row: warps 0-3, thread tid prefetching row tid (rows split over the
-    //    cluster's ranks) -- with KV sharing (B=8 H=64 S=131072: 284.7 ->
-    //    275.3 us) and in CTAs of a few blocks (B=8 H=16 S=8192: 19.1 -> 18.7);
+    //  * by row: warps 0-3, thread tid prefetching row tid -- in CTAs of a few
+    //    blocks (B=8 H=16 S=8192: 19.1 -> 18.7 us);
     //  * by line, over all seven gather warps -- in long unshared streams,
     //    where prefetching by row held up warps 0-3, which also issue gathers
     //    (B=8 H=16 S=131072: 139 us without a prefetch, 178 by row, 135 by line).
-    const bool pf_rows = CH > 1 || nblk <= kPrefetchMaxBlocks;
+    const bool pf_rows = nblk <= kPrefetchMaxBlocks;
     auto prefetch_block = [&](int j, int32_t v) {
         const int kb = k0 + j * kBlockN;
         const int nk = min(kBlockN, k1 - kb);
-        if (!pf_rows || !row_lane || tid >= nk || (tid % CH) != rank) return;
+        if (!pf_rows || !row_lane || tid >= nk) return;
         const bool ex = key_extra(kb + tid);
         if (!slot_ok(v, ex)) return;
         const uint8_t* row = (ex ? a.extra_pool : a.pool) + (int64_t)v * kWidth;
@@ -601,10 +584,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
     // ---- barriers and TMEM ----------------------------------------------------------------
     tc_fence_before();
-    if (CH > 1)
-        cluster_sync();   // peers' barriers are initialised before any multicast lands
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms.tmem_base;
     const uint32_t smem_base = smem_u32(smem);
@@ -736,12 +716,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                 b0 + (uint64_t)((kk * 512) >> 4), id_pv,
                                 (blk > 0 || kk > 0) ? 1u : 0u);
                 umma_commit_warp(&ms.pv_done[st]);
-                // the stage may be refilled once every CTA of the cluster is done
-                // with it (the last two blocks' stages are never refilled)
-                if (CH == 1)
-                    umma_commit_warp(&ms.kv_empty[st]);
-                else if (blk + 2 < nblk)
-                    umma_commit_multicast_warp(&ms.kv_empty[st], kClusterMask);
+                umma_commit_warp(&ms.kv_empty[st]);   // the stage may be refilled
             };
             auto issue_qk = [&](int blk) {
                 const int st = blk & 1;
@@ -1108,13 +1083,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
 
     // ---- teardown -------------------------------------------------------------------------------
-    // In a cluster no CTA leaves while a peer may still multicast into its
-    // stages or arrive on its barriers.
     tc_fence_before();
-    if (CH > 1)
-        cluster_sync();
-    else
-        __syncthreads();
+    __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -1123,50 +1093,32 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
 // ---- host side -------------------------------------------------------------------------------
 
-template <int N, bool SPARSE, int CH, bool EXTRA = false>
+template <int N, bool SPARSE, bool EXTRA = false>
 cudaError_t launch_variant(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
                            const mla_plan_t& plan, cudaStream_t stream)
 {
     constexpr int smem = smem_bytes<N, SPARSE>();
     static_assert(smem <= 227 * 1024, "one CTA's dynamic shared memory limit");
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(split_tc_kernel<N, SPARSE, CH, EXTRA>,
+    // The shared-memory opt-in is a per-device attribute of the kernel: set it
+    // once on every device this process launches on.
+    static DeviceOnce once;
+    cudaError_t e = once.run([] {
+        return cudaFuncSetAttribute(split_tc_kernel<N, SPARSE, EXTRA>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
-    if (attr != cudaSuccess) return attr;
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid_x, plan.grid_y, plan.grid_z);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute la[2];
+    cudaLaunchAttribute la[1];
     // a programmatic dependent of the preceding kernel: set-up overlaps its tail
     la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     la[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = 1;
-    if (CH > 1) {
-        // the CH head blocks of one (request, split) share every gathered block
-        la[1].id = cudaLaunchAttributeClusterDimension;
-        la[1].val.clusterDim.x = CH;
-        la[1].val.clusterDim.y = 1;
-        la[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
-    }
-    return cudaLaunchKernelEx(&cfg, split_tc_kernel<N, SPARSE, CH, EXTRA>, lat, rope, a);
-}
-
-template <bool SPARSE, bool EXTRA = false>
-cudaError_t launch_rows32(const CUtensorMap& lat, const CUtensorMap& rope, const SplitArgs& a,
-                          const mla_plan_t& plan, cudaStream_t stream)
-{
-    switch (plan.kv_share) {
-    case 2: return launch_variant<32, SPARSE, 2, EXTRA>(lat, rope, a, plan, stream);
-    case 4: return launch_variant<32, SPARSE, 4, EXTRA>(lat, rope, a, plan, stream);
-    default: return launch_variant<32, SPARSE, 1, EXTRA>(lat, rope, a, plan, stream);
-    }
+    return cudaLaunchKernelEx(&cfg, split_tc_kernel<N, SPARSE, EXTRA>, lat, rope, a);
 }
 
 }  // namespace
@@ -1219,15 +1171,15 @@ cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStre
         rope = lat;
     }
     if (a.sparse && a.extra_topk > 0) {
-        if (plan.rows_per_cta == 16) return launch_variant<16, true, 1, true>(lat, rope, a, plan, stream);
-        return launch_rows32<true, true>(lat, rope, a, plan, stream);
+        if (plan.rows_per_cta == 16) return launch_variant<16, true, true>(lat, rope, a, plan, stream);
+        return launch_variant<32, true, true>(lat, rope, a, plan, stream);
     }
     if (a.sparse) {
-        if (plan.rows_per_cta == 16) return launch_variant<16, true, 1>(lat, rope, a, plan, stream);
-        return launch_rows32<true>(lat, rope, a, plan, stream);
+        if (plan.rows_per_cta == 16) return launch_variant<16, true>(lat, rope, a, plan, stream);
+        return launch_variant<32, true>(lat, rope, a, plan, stream);
     }
-    if (plan.rows_per_cta == 16) return launch_variant<16, false, 1>(lat, rope, a, plan, stream);
-    return launch_rows32<false>(lat, rope, a, plan, stream);
+    if (plan.rows_per_cta == 16) return launch_variant<16, false>(lat, rope, a, plan, stream);
+    return launch_variant<32, false>(lat, rope, a, plan, stream);
 }
 
 }  // namespace mla

@@ -232,3 +232,91 @@ def workload_c4x(num_tokens: int, seed: int = 0, pool_rows: int = 131072, topk: 
     """Sparse top-k with a second (compressed) cache: the c4 shape plus, per
     token, ``extra_topk`` candidates of a ``extra_rows``-row second cache."""
     return sparse_extra_inputs(num_tokens, 64, topk, extra_topk, pool_rows, extra_rows, seed)
+
+
+# --- structured variants for precision-edge tests -----------------------------
+#
+# These reshape a workload's draws (scale parts of the queries, plant outliers,
+# copy rows) to build inputs whose numbers sit at the edges of the kernel's
+# number formats: wide dynamic range inside one query row, logits that are
+# nearly tied, logits far apart.  They only move and cast values; none of the
+# attention arithmetic happens here.
+
+def _queries(inp):
+    """(latent/NoPE part, RoPE part) of dense or sparse inputs."""
+    return (inp.q_lat, inp.q_pe) if isinstance(inp, DenseInputs) else (inp.q_nope, inp.q_pe)
+
+
+def _set_queries(inp, lat, pe):
+    if isinstance(inp, DenseInputs):
+        inp.q_lat = lat.to(torch.bfloat16).contiguous()
+    else:
+        inp.q_nope = lat.to(torch.bfloat16).contiguous()
+    inp.q_pe = pe.to(torch.bfloat16).contiguous()
+    return inp
+
+
+def scale_query_parts(inp, lat: float = 1.0, pe: float = 1.0):
+    """Multiply the latent (NoPE) and RoPE query parts by separate factors."""
+    ql, qp = _queries(inp)
+    return _set_queries(inp, ql.float() * lat, qp.float() * pe)
+
+
+def plant_query_outliers(inp, ratio: float, seed: int, part: str = "lat"):
+    """In every (row, head) query, one seeded column of the given part becomes
+    +-ratio while the other columns keep their N(0,1) draws."""
+    g = _gen(seed)
+    ql, qp = (t.float().clone() for t in _queries(inp))
+    tgt = ql if part == "lat" else qp
+    rows, heads, width = tgt.shape
+    col = torch.randint(0, width, (rows, heads), generator=g)
+    sign = torch.where(torch.rand(rows, heads, generator=g) < 0.5, -1.0, 1.0)
+    tgt.view(-1, width)[torch.arange(rows * heads), col.reshape(-1)] = (sign * ratio).reshape(-1)
+    return _set_queries(inp, ql, qp)
+
+
+def share_query_across_heads(inp):
+    """Every head of a query row gets head 0's query (all heads then rank the
+    keys alike)."""
+    ql, qp = _queries(inp)
+    return _set_queries(inp, ql[:, :1].expand_as(ql), qp[:, :1].expand_as(qp))
+
+
+def plant_dominant_key(inp: DenseInputs, strength: float, seed: int) -> DenseInputs:
+    """For each request, one seeded key's pool row becomes the e4m3fn cast of
+    strength * (that request's first query row, head 0) / kv_scale, so with
+    queries shared across heads its logit exceeds the others' by about
+    strength * |q|^2 * scale.  The other keys keep their draws."""
+    g = _gen(seed)
+    pool = inp.pool.clone()
+    width = pool.shape[-1]
+    for b in range(inp.batch):
+        n = int(inp.seq_lens[b])
+        if n == 0:
+            continue
+        j = int(torch.randint(0, n, (1,), generator=g))
+        slot = int(inp.kv_indices[int(inp.kv_indptr[b]) + j])
+        q = torch.cat([inp.q_lat[b * inp.q_len, 0].float(), inp.q_pe[b * inp.q_len, 0].float()])
+        row = (q * strength / inp.kv_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+        pool.view(-1, width)[slot] = row
+    inp.pool = pool
+    return inp
+
+
+def near_tied_pool(inp: DenseInputs, seed: int, flips: int = 4) -> DenseInputs:
+    """Every slot holds one base row (the pool's slot 0) with `flips` seeded
+    bytes moved to a neighbouring e4m3fn code, so all logits of a query are
+    tied up to a few tiny terms."""
+    g = _gen(seed)
+    width = inp.pool.shape[-1]
+    flat = inp.pool.view(-1, width)
+    base = flat[0].clone()
+    pool = base.unsqueeze(0).repeat(flat.shape[0], 1)
+    cols = torch.randint(0, width, (flat.shape[0], flips), generator=g)
+    rows = torch.arange(flat.shape[0]).unsqueeze(1).expand_as(cols)
+    mag = pool[rows, cols] & 0x7F
+    # step the magnitude code by one, staying inside finite non-NaN codes
+    stepped = torch.where(mag >= 0x7E, mag - 1, mag + 1)
+    pool[rows, cols] = (pool[rows, cols] & 0x80) | stepped
+    inp.pool = pool.view(inp.pool.shape).contiguous()
+    return inp

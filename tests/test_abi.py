@@ -175,27 +175,39 @@ def test_decode_rejects_unknown_variant(lib):
         assert _call_decode(lib, plan, ws_bytes=plan.workspace_bytes) == -1, variant
 
 
-def test_kv_share_choice(lib):
-    cases = [((8, 1, 16, 8 * 8192), 1), ((8, 4, 16, 8 * 8192), 2), ((2, 1, 64, 131072), 2),
-             ((64, 1, 128, 1081344), 4), ((1, 3, 40, 1537), 4), ((1, 2, 40, 100), 1),
-             ((3, 7, 5, 10), 2)]
-    for (batch, q_len, heads, keys), share in cases:
-        p = mla.mla_decode_plan(batch, q_len, heads, keys, 152)
-        assert p.kv_share == share, (batch, q_len, heads, p.kv_share)
-        assert p.head_blocks % p.kv_share == 0
-    assert mla.mla_sparse_decode_plan(4, 64, 2048, 152).kv_share == 2
-    assert mla.mla_sparse_decode_plan(4, 128, 2048, 152).kv_share == 4
-    assert mla.mla_sparse_decode_plan(4, 16, 2048, 152).kv_share == 1
+def test_every_plan_gathers_its_own_rows(lib):
+    # each CTA gathers its own KV rows (no cluster sharing): kv_share is 1
+    for batch, q_len, heads, keys in [(8, 1, 16, 8 * 8192), (8, 4, 16, 8 * 8192),
+                                      (2, 1, 64, 131072), (64, 1, 128, 1081344),
+                                      (1, 3, 40, 1537), (3, 7, 5, 10)]:
+        assert mla.mla_decode_plan(batch, q_len, heads, keys, 152).kv_share == 1
+    for heads in (16, 64, 128):
+        assert mla.mla_sparse_decode_plan(4, heads, 2048, 152).kv_share == 1
 
 
-def test_decode_rejects_inconsistent_kv_share(lib):
-    p16 = mla.mla_decode_plan(1, 1, 16, 4096, 152)    # 16 rows per CTA
-    p64 = mla.mla_decode_plan(1, 1, 64, 4096, 152)    # 2 head blocks of 32
-    for plan, share in [(p16, 2), (p64, 4), (p64, 3), (p64, 0), (p64, 8)]:
-        q = mla.mla_plan_t.from_buffer_copy(plan)
+def test_decode_rejects_kv_share_other_than_one(lib):
+    p64 = mla.mla_decode_plan(1, 1, 64, 4096, 152)
+    for share in (0, 2, 4, 8):
+        q = mla.mla_plan_t.from_buffer_copy(p64)
         q.kv_share = share
-        heads = q.num_heads
-        assert _call_decode(lib, q, ws_bytes=q.workspace_bytes, heads=heads) == -1, share
+        assert _call_decode(lib, q, ws_bytes=q.workspace_bytes, heads=64) == -1, share
+
+
+def test_decode_rejects_a_plan_whose_fields_disagree(lib):
+    # the kernels index the workspace and outputs by the plan's geometry, so a
+    # plan edited out of step with its shape is refused before any launch
+    base = mla.mla_plan_force_splits(mla.mla_decode_plan(2, 1, 64, 8192, 152), 4)
+    edits = [("workspace_bytes", base.workspace_bytes - 256),      # stale size
+             ("workspace_bytes", base.workspace_bytes + 256),
+             ("grid_y", 5), ("grid_x", 1), ("grid_z", 3), ("head_blocks", 1),
+             ("rows_per_cta", 16), ("block_n", 64)]
+    for field, value in edits:
+        q = mla.mla_plan_t.from_buffer_copy(base)
+        setattr(q, field, value)
+        rc = _call_decode(lib, q, ws_bytes=1 << 30, batch=2, heads=64)
+        assert rc == -1, (field, value, rc)
+    # the untouched plan passes every host check (and then needs a device)
+    assert _call_decode(lib, base, ws_bytes=1 << 30, batch=2, heads=64) not in (-1, -3, -4)
 
 
 @pytest.mark.parametrize("tokens,splits", [(1, 16), (8, 8), (24, 2), (64, 1)])
@@ -217,10 +229,10 @@ def test_long_first_only_when_the_grid_outlasts_a_wave():
 @pytest.mark.parametrize("batch,q_len,heads,keys_per_request,splits", [
     (8, 1, 16, 8192, 16),       # c1 q_len=1
     (8, 4, 16, 8192, 8),        # c1 q_len=4
-    (8, 1, 64, 131072, 19),     # c2 8x131072 (two full waves of clusters)
+    (8, 1, 64, 131072, 19),     # c2 8x131072 (two full waves)
     (1, 1, 64, 131072, 74),     # c2 1x131072
     (16, 1, 64, 131072, 19),    # c2 16x131072
-    (64, 1, 128, 16896, 1),     # c3's shape (mean length)
+    (64, 1, 128, 16896, 4),     # c3's shape (mean length)
 ])
 def test_dense_plan_stays_within_the_measured_best(batch, q_len, heads, keys_per_request,
                                                    splits):

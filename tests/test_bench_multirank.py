@@ -99,3 +99,56 @@ def test_packed_buffers_are_256_byte_aligned_views():
         v.copy_(t)
     for v, t in zip(views, ts):
         assert torch.equal(v, t)
+
+
+def _gloo_max(argv):
+    # a spawn_ranks target: the rank's environment is set as torchrun sets it
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo")
+    try:
+        rank, world = dist.get_rank(), dist.get_world_size()
+        assert int(os.environ["LOCAL_RANK"]) == rank and world == int(os.environ["WORLD_SIZE"])
+        got = bench.max_over_ranks(10.0 + rank, world, "cpu")
+        with open(os.path.join(argv[0], f"rank{rank}"), "w") as f:
+            f.write(f"{world} {got}")
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_spawn_ranks_runs_one_process_per_rank_with_torchrun_env(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+    bench.spawn_ranks(2, [str(tmp_path)], target=_gloo_max)
+    assert sorted(os.listdir(tmp_path)) == ["rank0", "rank1"]
+    for r in (0, 1):
+        assert open(tmp_path / f"rank{r}").read() == "2 11.0"
+
+
+def test_bench_gpus_2_spawns_ranks_and_prints_one_line():
+    # `bench.py --gpus 2` without torchrun launches two ranks itself; the
+    # reference arm runs on rank 0 only, so exactly one JSON line comes out
+    import json
+    import subprocess
+    env = dict(os.environ)
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--workload", "c0", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
+
+
+def test_every_sweep_workload_name_parses():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.ALL_WORKLOADS[1] == "c1q1"
+    for name in bench.ALL_WORKLOADS:
+        if name.startswith(("c2-", "c3")):
+            continue   # large pools; the names share their parser with c2-2x4096 above
+        k, inp, desc = bench.make_workload(name)
+        assert desc

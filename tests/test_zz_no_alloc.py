@@ -63,12 +63,19 @@ def test_noalloc_matches_mla_decode_on_two_calls_in_a_row():
 def test_noalloc_rejects_plans_beyond_its_scratch():
     mla.load()
     inp = gen.workload_c0()
-    plan = mla.mla_decode_plan(1, 1, 16, 256, mla.sm_count())
-    big = mla.mla_plan_force_splits(plan, 256)
-    big.batch, big.q_len, big.num_heads = 1, 1, 16
-    big.workspace_bytes = mla.MLA_NOALLOC_SCRATCH_BYTES + 1
     q_lat, q_pe, pool, lens, idx, ptr = _device(inp)
     o = torch.empty_like(q_lat)
+    # a shape whose partials need more than the scratch holds
+    big = mla.mla_plan_force_splits(mla.mla_decode_plan(64, 1, 128, 64 * 4096, mla.sm_count()),
+                                    256)
+    assert big.workspace_bytes > mla.MLA_NOALLOC_SCRATCH_BYTES
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_noalloc(big, q_lat, q_pe, pool, lens, idx, ptr, inp.scale,
+                               inp.kv_scale, o)
+    assert e.value.status == -4
+    # a plan whose workspace_bytes field was edited down is judged by its shape,
+    # not by the field: still too big for the scratch
+    big.workspace_bytes = 1024
     with pytest.raises(mla.MlaError) as e:
         mla.mla_decode_noalloc(big, q_lat, q_pe, pool, lens, idx, ptr, inp.scale,
                                inp.kv_scale, o)

@@ -77,8 +77,10 @@ extern "C" {
 /* Largest split count the reducer accepts (hip_mha_decoding_num_partitions: the
  * reducer's 256-partition specialization caps the MLA-style split count). */
 #define MLA_MAX_SPLITS 256
-/* Bytes at the start of every workspace that hold the device error word. */
-#define MLA_WORKSPACE_HEADER_BYTES 256
+/* Bytes at the start of every workspace that hold the device error word and
+ * the fused merge's arrival tickets; zero them before a workspace's first use
+ * (mla_workspace_reset does). */
+#define MLA_WORKSPACE_HEADER_BYTES 65536
 
 /*
  * A launch plan: a pure function of shapes and the SM count (README, "MLA
@@ -110,7 +112,17 @@ typedef struct {
                                 request (ties by index), so the longest work is
                                 scheduled first; set when the grid outlasts one
                                 wave and batch <= 256; results do not depend on it */
-    int32_t reserved;        /* 0 */
+    int32_t merge_cluster;   /* 1: the split-K merge is a second kernel (the split-K
+                                reduce); 2 or 4: it is fused into the split kernel,
+                                whose CTAs form clusters of that many consecutive
+                                splits (num_splits a multiple of it) that merge
+                                their partials through each other's shared memory,
+                                the last cluster of a tile to finish merging the
+                                clusters' results; results do not depend on the
+                                timing.  The planner fuses only when one cluster
+                                holds all of a tile's splits; larger split counts
+                                may be fused by setting it (see
+                                mla_plan_force_splits) */
 } mla_plan_t;
 
 /*
@@ -332,9 +344,13 @@ int mla_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
 
 /*
  * Re-target a plan to a forced split count (1..MLA_MAX_SPLITS), updating its
- * grid and workspace size.  For split sweeps (moonmath-ai/amd-kernels README,
- * "Results -- MLA decode": num_kv_splits swept per shape) and tests; the
- * planner's own choice needs no call to it.
+ * grid, its merge cluster size (as the planner sets it: the fused merge when
+ * num_splits is 2 or 4 and one cluster then holds all of a tile's splits,
+ * else 1) and its workspace size.  For split sweeps
+ * (moonmath-ai/amd-kernels README, "Results -- MLA decode": num_kv_splits swept
+ * per shape) and tests; the planner's own choice needs no call to it.  A
+ * caller may set merge_cluster to 1 afterwards (the separate reduce) or to
+ * another size that fits; the decode calls reject one that does not.
  */
 int mla_plan_force_splits(mla_plan_t* plan, int32_t num_splits);
 

@@ -28,13 +28,35 @@ inline int32_t rows_per_cta_for(int64_t rows) { return rows <= 16 ? 16 : 32; }
 constexpr double kBlockUs = 1.65;      // 128 x 576 B at one SM's share of HBM bandwidth
 constexpr double kCtaUs = 2.0;         // prologue, pipeline fill, epilogue
 constexpr double kReduceUs = 2.0;      // reduce launch and its latency chain
+constexpr double kFusedUs = 0.6;       // fused merge: two cluster barriers and the slice merge
+constexpr double kTicketUs = 3.0;      // ... plus, with several clusters, ticket and L2 round trips
 constexpr double kBytesPerUs = 6.8e6;  // HBM bytes per microsecond
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
-// CTAs resident at once: one per SM.
-int64_t wave_ctas(int32_t sm_count) { return sm_count; }
+// CTAs resident at once, one per SM, in clusters of `mc` (GB300, measured with
+// cudaOccupancyMaxActiveClusters at this kernel's shared memory: clusters of 2
+// fill all 152 SMs, clusters of 4 leave 8 idle).
+int64_t wave_ctas(int32_t sm_count, int32_t mc = 1)
+{
+    return mc >= 4 ? (int64_t)sm_count - sm_count / 19 : sm_count;
+}
+
+// Merge cluster sizes the split kernel is built for, largest first.
+constexpr int32_t kMergeClusters[] = {4, 2};
+
+// Whether clusters of `mc` splits can fuse the merge of a plan: the split count
+// divides into clusters, every (tile, rank) has a ticket, and a CTA of the last
+// cluster merges at most kMaxMergeTerms (row, cluster) partials.
+bool fused_merge_ok(int64_t tiles, int32_t ns, int32_t rows_per_cta, int32_t mc)
+{
+    if (mc != 2 && mc != 4) return false;
+    if (ns < mc || ns % mc != 0 || rows_per_cta % mc != 0) return false;
+    if (tiles * mc > kMaxTickets) return false;
+    const int64_t nclus = ns / mc;
+    return nclus == 1 || nclus * (rows_per_cta / mc) <= kMaxMergeTerms;
+}
 
 int device_ok()
 {
@@ -64,27 +86,51 @@ int64_t workspace_for(int64_t items, int ns, int d_v)
     return bytes;
 }
 
-// Split count for `tiles` (request, head block) tiles, `keys` keys per
-// request and `items` output rows (row x head) in the call.
-int32_t gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v, int32_t sm_count)
+// The merge cluster size the planner uses for a split count: the fused merge
+// when one cluster holds all of a tile's splits (ns of 2 or 4), else 1 (the
+// separate reduce).
+int32_t planned_merge_cluster(int64_t tiles, int32_t ns, int32_t rows_per_cta)
+{
+    for (int32_t mc : kMergeClusters)
+        if (ns == mc && fused_merge_ok(tiles, ns, rows_per_cta, mc)) return mc;
+    return 1;
+}
+
+struct SplitChoice {
+    int32_t ns, mc;
+};
+
+// Split count and merge cluster size for `tiles` (request, head block) tiles
+// of `rows_per_cta` rows, `keys` keys per request and `items` output rows (row
+// x head) in the call: the cheapest by the cost model, over every split count
+// with the separate reduce and every fused-merge cluster size that fits.
+SplitChoice gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v,
+                         int32_t sm_count, int32_t rows_per_cta)
 {
     const int64_t blocks = ceil_div(keys > 0 ? keys : 1, kBlockN);
     const int64_t ctas = tiles > 0 ? tiles : 1;
     const int64_t max_ns = blocks < MLA_MAX_SPLITS ? blocks : MLA_MAX_SPLITS;
-    const double block_us = kBlockUs;
-    const int64_t wave = wave_ctas(sm_count);
     double best = 0.0;
-    int32_t best_ns = 1;
-    for (int64_t ns = 1; ns <= max_ns; ++ns) {
-        const double waves = (double)ceil_div(ctas * ns, wave);
-        double t = waves * ((double)ceil_div(blocks, ns) * block_us + kCtaUs);
-        if (ns > 1) t += kReduceUs + (double)items * ns * d_v * 4.0 * 2.0 / kBytesPerUs;
-        if (ns == 1 || t < best - 1e-9) {
+    SplitChoice pick{1, 1};
+    auto consider = [&](int64_t ns, int32_t mc) {
+        const double waves = (double)ceil_div(ctas * ns, wave_ctas(sm_count, mc));
+        double t = waves * ((double)ceil_div(blocks, ns) * kBlockUs + kCtaUs);
+        if (ns > 1 && mc == 1) t += kReduceUs + (double)items * ns * d_v * 4.0 * 2.0 / kBytesPerUs;
+        if (mc > 1) t += kFusedUs + (ns > mc ? kTicketUs : 0.0);
+        if ((pick.ns == 1 && pick.mc == 1 && ns == 1) || t < best - 1e-9) {
             best = t;
-            best_ns = (int32_t)ns;
+            pick = SplitChoice{(int32_t)ns, mc};
         }
+    };
+    for (int64_t ns = 1; ns <= max_ns; ++ns) {
+        consider(ns, 1);
+        // the fused merge only where one cluster holds every split of a tile:
+        // measured on GB300, a tile of several clusters (ticket, then a merge
+        // of the clusters' partials from L2) costs more than the reduce kernel
+        for (int32_t mc : kMergeClusters)
+            if (ns == mc && fused_merge_ok(ctas, (int32_t)ns, rows_per_cta, mc)) consider(ns, mc);
     }
-    return best_ns;
+    return pick;
 }
 
 // Sparse split rule, following flashinfer.mla.cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits
@@ -113,7 +159,7 @@ int32_t sparse_splits(int64_t ctas, int64_t topk, int32_t sm_count)
 }
 
 void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32_t d_v,
-               int32_t d_rope, int32_t sm_count, int64_t total_keys, int32_t ns)
+               int32_t d_rope, int32_t sm_count, int64_t total_keys, int32_t ns, int32_t mc)
 {
     const int32_t rows = q_len * heads;
     std::memset(p, 0, sizeof *p);
@@ -134,6 +180,7 @@ void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32
     p->sm_count = sm_count;
     p->total_keys = total_keys;
     p->kv_share = 1;
+    p->merge_cluster = mc;
 }
 
 }  // namespace
@@ -184,17 +231,26 @@ bool variant_ok(const mla_plan_t* plan)
         plan->grid_x != plan->head_blocks || plan->grid_y != plan->num_splits ||
         plan->grid_z != plan->batch)
         return false;
+    if (plan->merge_cluster != 1 &&
+        !fused_merge_ok((int64_t)plan->batch * plan->head_blocks, plan->num_splits,
+                        plan->rows_per_cta, plan->merge_cluster))
+        return false;
     if (plan->long_first != 0 && (plan->long_first != 1 || plan->batch > kLongFirstMaxBatch))
         return false;
     return plan->kv_share == 1;
 }
 
+// The split kernel, then the split-K reduce when the plan has several splits
+// and does not fuse the merge.  Without the reduce (the *_splits entry points)
+// the kernel leaves every split's partial in the workspace.
 int run(const mla_plan_t* plan, SplitArgs& a, int64_t items, cudaStream_t stream,
         bool with_reduce)
 {
-    cudaError_t e = launch_split_tc(a, *plan, stream);
+    const int mc = with_reduce ? plan->merge_cluster : 1;
+    a.tickets = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(a.err) + kErrorAreaBytes);
+    cudaError_t e = launch_split_tc(a, *plan, mc, stream);
     if (e != cudaSuccess) return MLA_ERR_LAUNCH_FAILED;
-    if (with_reduce && plan->num_splits > 1) {
+    if (with_reduce && mc == 1 && plan->num_splits > 1) {
         void* out = a.o_f32 ? static_cast<void*>(a.o_f32) : static_cast<void*>(a.o);
         e = launch_splitk_reduce(a.o_part, a.lse_part, items, plan->num_splits, plan->d_v,
                                  a.out_scale, out, a.o_f32 != nullptr, a.lse, stream);
@@ -250,14 +306,15 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
     if (rows > (1 << 20)) return MLA_ERR_UNSUPPORTED_SHAPE;
     const int64_t head_blocks = ceil_div(rows, rows_per_cta_for(rows));
     const int64_t keys = batch > 0 ? ceil_div(total_keys, batch) : 0;
-    const int32_t ns = gb300_splits(head_blocks * (batch > 0 ? batch : 1), keys,
-                                    (int64_t)batch * rows, d_v, sm_count);
-    fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ns);
+    const SplitChoice ch = gb300_splits(head_blocks * (batch > 0 ? batch : 1), keys,
+                                        (int64_t)batch * rows, d_v, sm_count,
+                                        rows_per_cta_for(rows));
+    fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ch.ns, ch.mc);
     // Longest requests first once the grid outlasts one wave (variable lengths
     // then leave the short requests for the last wave).
     const int64_t ctas = (int64_t)out->grid_x * out->grid_y * out->grid_z;
     out->long_first = (batch >= 2 && batch <= kLongFirstMaxBatch &&
-                       ctas > wave_ctas(sm_count)) ? 1 : 0;
+                       ctas > wave_ctas(sm_count, ch.mc)) ? 1 : 0;
     return MLA_OK;
 }
 
@@ -276,8 +333,10 @@ int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
     int32_t ns = sparse_splits(head_blocks * (num_tokens > 0 ? num_tokens : 1),
                                (int64_t)topk + extra_topk, sm_count);
     if (ns > cap) ns = cap;
+    const int32_t rpc = rows_per_cta_for(num_heads);
     fill_plan(out, num_tokens, 1, num_heads, d_v, d_rope, sm_count,
-              (int64_t)num_tokens * ((int64_t)topk + extra_topk), ns);
+              (int64_t)num_tokens * ((int64_t)topk + extra_topk), ns,
+              planned_merge_cluster(head_blocks * num_tokens, ns, rpc));
     out->extra_topk = extra_topk;
     return MLA_OK;
 }
@@ -558,6 +617,8 @@ int mla_plan_force_splits(mla_plan_t* plan, int32_t num_splits)
     if (plan->q_len < 1 || plan->num_heads < 1 || plan->batch < 0) return MLA_ERR_INVALID_ARG;
     plan->num_splits = num_splits;
     plan->grid_y = num_splits;
+    plan->merge_cluster = planned_merge_cluster((int64_t)plan->batch * plan->head_blocks,
+                                                num_splits, plan->rows_per_cta);
     plan->workspace_bytes = workspace_for((int64_t)plan->batch * plan->q_len * plan->num_heads,
                                           num_splits, plan->d_v);
     return MLA_OK;

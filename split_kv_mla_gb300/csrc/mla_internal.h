@@ -77,7 +77,18 @@ struct SplitArgs {
     const int32_t* glen = nullptr;
     int32_t cp_rank = 0;
     int32_t cp_world = 1;
+    // fused merge (plan.merge_cluster > 1): per (request x head block, cluster
+    // rank) arrival tickets in the workspace header, zero between calls
+    uint32_t* tickets = nullptr;
 };
+
+// Merge-ticket counters in the workspace header: after the 256-byte error-word
+// area, one uint32 per (tile, cluster rank) of a fused-merge launch.
+constexpr int64_t kErrorAreaBytes = 256;
+constexpr int64_t kMaxTickets = (MLA_WORKSPACE_HEADER_BYTES - kErrorAreaBytes) / 4;
+// Largest number of (row, cluster) partials one CTA of the last cluster merges
+// from the workspace in a fused merge (its slice rows x the tile's clusters).
+constexpr int kMaxMergeTerms = 32;
 
 // Kernel variants (mla_plan_t::variant).  Value 1 belonged to a CUDA-core
 // bring-up kernel that the tcgen05 kernel replaced; it is rejected.
@@ -85,7 +96,9 @@ enum Variant : int32_t {
     kVariantTc = 2,   // tcgen05 + TMA split kernel, then the split-K reduce kernel
 };
 
-cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, cudaStream_t stream);
+// The split kernel; mc > 1 fuses the split-K merge (clusters of mc splits).
+cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, int mc,
+                            cudaStream_t stream);
 
 // Workspace bytes that a plan needs, recomputed from its shape and split count.
 int64_t needed_workspace(const mla_plan_t* plan);

@@ -184,6 +184,43 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Address, in the shared::cluster window, of the variable at p's offset in the
+// shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// 16 bytes (addr 16-byte aligned).
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Atomic add with acquire-release ordering at GPU scope; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // ---- tensor memory ---------------------------------------------------------------------------
 
 // Allocate ncols (power of two >= 32) TMEM columns; the base address is

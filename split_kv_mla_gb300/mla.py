@@ -23,7 +23,7 @@ _lock = threading.Lock()
 
 MLA_OK = 0
 MLA_MAX_SPLITS = 256
-MLA_WORKSPACE_HEADER_BYTES = 256
+MLA_WORKSPACE_HEADER_BYTES = 65536
 MLA_DEVERR_BAD_SLOT = 1
 MLA_DEVERR_TIMEOUT = 2
 MLA_DEVERR_BAD_LENGTH = 4
@@ -48,7 +48,7 @@ class mla_plan_t(ctypes.Structure):
         ("d_v", ctypes.c_int32), ("d_rope", ctypes.c_int32), ("sm_count", ctypes.c_int32),
         ("total_keys", ctypes.c_int64), ("kv_share", ctypes.c_int32),
         ("extra_topk", ctypes.c_int32), ("long_first", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("merge_cluster", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -175,6 +175,9 @@ def test_splits_then_reduce_equals_the_one_call():
     sl, si, sp, glen = dcp.shard_page_table(d["seq_lens"], d["kv_indices"], d["kv_indptr"], 1, 2)
     plan = mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads, si.numel(), mla.sm_count())
     plan = mla.mla_plan_force_splits(plan, 4)
+    # the one call with the separate reduce is exactly split kernel + reduce
+    # (a fused merge associates the same terms differently)
+    plan.merge_cluster = 1
     args = (plan, d["q_lat"], d["q_pe"], d["pool"], sl, si, sp, inp.scale, inp.kv_scale,
             glen, 1, 2)
     ws = mla.workspace(plan)

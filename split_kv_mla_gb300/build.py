@@ -57,14 +57,17 @@ def _compile(src: str, obj: str, extra) -> None:
         sys.stderr.write(r.stderr)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), build_dir: str = BUILD) -> str:
+    """Compile every csrc/*.cu (extra nvcc flags appended) into build_dir and
+    link build_dir/libmla.so; returns the library's path."""
+    lib = os.path.join(build_dir, "libmla.so")
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = _headers()
     jobs = []
     objs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *headers]):
             jobs.append((src, obj))
@@ -73,18 +76,18 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
             futs = [ex.submit(_compile, s, o, list(extra)) for s, o in jobs]
             for f in futs:
                 f.result()
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         libdir = _cuda_lib_dir()
         cmd = [_nvcc(), *ARCH, "-shared", "-cudart=shared", "-o", tmp, *objs,
                "-L", libdir, "-Xlinker", "-rpath=" + libdir]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     if verbose:
-        print(LIB)
-    return LIB
+        print(lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -80,7 +80,21 @@ struct SplitArgs {
     // fused merge (plan.merge_cluster > 1): per (request x head block, cluster
     // rank) arrival tickets in the workspace header, zero between calls
     uint32_t* tickets = nullptr;
+    // phase time stamps (builds with MLA_TRACE only): kTraceSlots per CTA
+    unsigned long long* trace = nullptr;
 };
+
+// Phase stamps of a traced build (compiled with -DMLA_TRACE): per CTA of the
+// split kernel, globaltimer nanoseconds at kTraceSlots points, for at most
+// kTraceCtas CTAs (linear CTA index x + grid_x (y + grid_y z)).
+constexpr int kTraceSlots = 12;
+constexpr int kTraceCtas = 8192;
+// ... followed by per-block events of the first kTraceBlockCtas CTAs.
+constexpr int kTraceBlockCtas = 4;
+constexpr int kTraceBlocks = 64;
+constexpr int kTraceBlockEvents = 6;
+constexpr int kTraceWords =
+    kTraceCtas * kTraceSlots + kTraceBlockCtas * kTraceBlocks * kTraceBlockEvents;
 
 // Merge-ticket counters in the workspace header: after the 256-byte error-word
 // area, one uint32 per (tile, cluster rank) of a fused-merge launch.

@@ -76,6 +76,39 @@
 namespace mla {
 namespace {
 
+// Phase stamps of a traced build: slot i of this CTA gets the global timer.
+#ifdef MLA_TRACE
+__device__ __forceinline__ void trace_stamp(const SplitArgs& a, int i)
+{
+    const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (a.trace == nullptr || cta >= (unsigned)kTraceCtas) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    a.trace[(size_t)cta * kTraceSlots + i] = t;
+}
+#define MLA_STAMP(i) trace_stamp(a, (i))
+// Per-block events of the first kTraceBlockCtas CTAs: block j, event e.
+__device__ __forceinline__ void trace_block(const SplitArgs& a, int j, int e)
+{
+    const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (a.trace == nullptr || cta >= (unsigned)kTraceBlockCtas || j >= kTraceBlocks) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    a.trace[(size_t)kTraceCtas * kTraceSlots +
+            ((size_t)cta * kTraceBlocks + j) * kTraceBlockEvents + e] = t;
+}
+#define MLA_BLOCK_STAMP(j, e) trace_block(a, (j), (e))
+#else
+#define MLA_STAMP(i) ((void)0)
+#define MLA_BLOCK_STAMP(j, e) ((void)0)
+#endif
+// Block events: 0 gather warp 0 starts issuing the block, 1 it has issued its
+// copies, 2 QK issued, 3 S loaded by the first softmax warp, 4 its P
+// published, 5 P.V issued.
+// Stamp slots: 0 CTA start, 1 after the wait for the preceding kernel,
+// 2 first gather issued, 3 first QK issued, 4 last P.V issued, 5 epilogue has
+// O, 6 rows staged, 7 rows stored, 8 end.
+
 
 using namespace sm100;
 
@@ -552,6 +585,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     // every CTA of this grid has started; it waits for this grid's completion
     // before reading anything.
     asm volatile("griddepcontrol.launch_dependents;");
+    if (tid == 0) MLA_STAMP(0);
     const int rows_in_req = a.q_len * a.num_heads;
 
     // kv_empty: the stage's P.V has finished and it may be refilled; pv_done:
@@ -579,6 +613,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     // still be writing the inputs (queries, page table, cache rows): wait for it
     // before the first global read.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) MLA_STAMP(1);
 
     // Longest requests first.  With more CTAs than one wave, grid slice z takes
     // the z-th request in decreasing length order (ties in index order): the
@@ -848,8 +883,17 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
     if (warp < kGatherWarps && nblk > 0) {
         // start the first two blocks before anything else
+        if (tid == 0) MLA_BLOCK_STAMP(0, 0);
         issue(0, fix_slots(s0), row_valid(0, w0));
-        if (nblk > 1) issue(1, fix_slots(s1), row_valid(1, w1));
+        if (tid == 0) {
+            MLA_STAMP(2);
+            MLA_BLOCK_STAMP(0, 1);
+        }
+        if (nblk > 1) {
+            if (tid == 0) MLA_BLOCK_STAMP(1, 0);
+            issue(1, fix_slots(s1), row_valid(1, w1));
+            if (tid == 0) MLA_BLOCK_STAMP(1, 1);
+        }
         if (nblk > 2) {
             prefetch_block(2, rnext);
             pf_lines_issue(2, lpf2);
@@ -942,7 +986,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         for (int j = 2; j < nblk; ++j) {
             if (!warp_wait(&ms.kv_empty[j & 1], ((j - 2) >> 1) & 1, abort_flag, kGatherSleepNs))
                 break;
+            if (tid == 0) MLA_BLOCK_STAMP(j, 0);
             issue(j, fix_slots(gnext), row_valid(j, rnext));
+            if (tid == 0) MLA_BLOCK_STAMP(j, 1);
             issued = j + 1;
             if (j + 1 < nblk) {
                 gnext = raw_slots(j + 1);
@@ -1029,7 +1075,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 if (next_pv < next_qk && ready(&ms.p_full[next_pv & 1], (next_pv >> 1) & 1)) {
                     tc_fence_after();
                     issue_pv(next_pv);
-                    if (next_pv == nblk - 1) umma_commit_warp(&ms.o_done);
+                    if (lane == 0) MLA_BLOCK_STAMP(next_pv, 5);
+                    if (next_pv == nblk - 1) {
+                        umma_commit_warp(&ms.o_done);
+                        if (lane == 0) MLA_STAMP(4);
+                    }
                     ++next_pv;
                     did = true;
                 }
@@ -1037,6 +1087,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                     (next_qk < 2 || ready(&ms.s_free[next_qk & 1], ((next_qk - 2) >> 1) & 1))) {
                     tc_fence_after();
                     issue_qk(next_qk);
+                    if (lane == 0) MLA_BLOCK_STAMP(next_qk, 2);
+                    if (next_qk == 0 && lane == 0) MLA_STAMP(3);
                     ++next_qk;
                     did = true;
                 }
@@ -1095,6 +1147,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 const uint32_t sa = tmem + lane_addr + C::kColS + st * NQ + r0;
                 if (q3) load_rows<R>(sa, sa + N, sa + 2 * N, s);
                 else load_rows<R>(sa, sa + N, s);
+                if (warp == kSoftmaxWarp0 && lane == 0) MLA_BLOCK_STAMP(blk, 3);
             } else {
 #pragma unroll
                 for (int n = 0; n < R; ++n) s[n] = -CUDART_INF_F;
@@ -1230,6 +1283,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.p_full[st]);
+            if (warp == kSoftmaxWarp0 && lane == 0) MLA_BLOCK_STAMP(blk, 4);
             // Running sums of this warp's 32 keys (lane ends up with set row
             // my_row).  The empty asm keeps the compiler from scheduling these
             // shuffles ahead of the P hand-off above, where they would delay the MMA.
@@ -1268,6 +1322,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 : -1;
         }
         const bool have_o = alive && nblk > 0 && warp_wait(&ms.o_done, 0, abort_flag);
+        if (warp == kSoftmaxWarp0 && lane == 0) MLA_STAMP(5);
         if (have_o) tc_fence_after();
         softmax_bar(bar_id);
         // One split writes the final rows: bf16 into o, or fp32 into o_f32 when
@@ -1338,6 +1393,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
         fence_proxy_async_smem();
         softmax_bar(bar_id);
+        if (warp == kSoftmaxWarp0 && lane == 0) MLA_STAMP(6);
         // (a fused merge reads the staged partials from shared memory instead)
         if (MC == 1 && ti < R) {
             const int row = r0 + ti;
@@ -1357,6 +1413,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 bulk_wait_read();
             }
         }
+        if (warp == kSoftmaxWarp0 && lane == 0) MLA_STAMP(7);
         if ((!alive || *abort_flag) && lane == 0) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
     }
 
@@ -1368,6 +1425,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         tmem_dealloc(tmem, C::kTmemCols);
     }
     if constexpr (MC > 1) fused_merge<N, SPARSE, MC>(smem, ms, a, b, hb, split);
+    if (tid == kSoftmaxWarp0 * 32) MLA_STAMP(8);
 }
 
 // ---- host side -------------------------------------------------------------------------------

@@ -45,9 +45,19 @@ bool make_row_map(CUtensorMap* m, const void* pool, int64_t rows, int row_bytes,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, int mc,
+#ifdef MLA_TRACE
+// Phase stamps of the last split-kernel launch (traced builds only).
+static __device__ unsigned long long g_trace[kTraceWords];
+#endif
+
+cudaError_t launch_split_tc(const SplitArgs& a_in, const mla_plan_t& plan, int mc,
                             cudaStream_t stream)
 {
+    SplitArgs a = a_in;
+#ifdef MLA_TRACE
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&a.trace), g_trace) != cudaSuccess)
+        a.trace = nullptr;
+#endif
     if (plan.grid_x <= 0 || plan.grid_y <= 0 || plan.grid_z <= 0) return cudaSuccess;
     CUtensorMap lat, rope;
     const int row_bytes = a.d_v + a.d_rope;
@@ -68,3 +78,28 @@ cudaError_t launch_split_tc(const SplitArgs& a, const mla_plan_t& plan, int mc,
 }
 
 }  // namespace mla
+
+#ifdef MLA_TRACE
+// Traced builds: copy the phase stamps of the last split-kernel launch
+// (kTraceCtas x kTraceSlots globaltimer values, then the per-block events of
+// the first CTAs; zero where none was written)
+// to host memory; synchronises the device.
+extern "C" int mla_trace_read(unsigned long long* host, int64_t count)
+{
+    if (!host || count < 0 || count > (int64_t)mla::kTraceWords)
+        return MLA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+    return cudaMemcpyFromSymbol(host, mla::g_trace, count * sizeof(unsigned long long)) ==
+                   cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
+}
+
+// Traced builds: zero the stamps.
+extern "C" int mla_trace_clear(void)
+{
+    static unsigned long long zeros[mla::kTraceWords];
+    return cudaMemcpyToSymbol(mla::g_trace, zeros, sizeof zeros) == cudaSuccess ? MLA_OK
+                                                                                 : MLA_ERR_CUDA;
+}
+#endif

@@ -59,13 +59,15 @@ def library_path() -> str:
     return _build.LIB
 
 
-def load(build_if_missing: bool = True):
-    """Load libmla.so (building it first if it is missing and nvcc exists)."""
+def load(build_if_missing: bool = True, path: Optional[str] = None):
+    """Load libmla.so (building it first if it is missing and nvcc exists), or
+    the library at `path` (a variant build, e.g. the traced one) if given
+    before the first load."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB
+        path = path or _build.LIB
         if not os.path.exists(path):
             if not build_if_missing:
                 raise OSError(f"libmla.so not built ({path})")

@@ -232,6 +232,17 @@ __device__ __forceinline__ int q_shift(float amax)
     return 8 - e;
 }
 
+// Packed e4m3x2 -> two fp32 through the conversion unit (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2_cvt(uint16_t v)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    float lo, hi;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
+}
+
 // Split two fp32 values into e4m3 hi bytes and e4m3 bytes of the residual
 // times 2^kLoBits (pairs packed lo-byte first); returns the values the pairs
 // represent, hi + lo * 2^-kLoBits (exact in fp32: the subtraction and the
@@ -242,9 +253,9 @@ __device__ __forceinline__ float2 split_pair(float a, float b, uint16_t& hi, uin
     constexpr float up = (float)(1 << kLoBits);
     constexpr float back = 1.f / up;
     hi = f32x2_to_e4m3x2(a, b);
-    const float2 h = e4m3x2_to_f32x2((uint32_t)hi);
+    const float2 h = e4m3x2_to_f32x2_cvt(hi);
     lo = f32x2_to_e4m3x2((a - h.x) * up, (b - h.y) * up);
-    const float2 l = e4m3x2_to_f32x2((uint32_t)lo);
+    const float2 l = e4m3x2_to_f32x2_cvt(lo);
     return make_float2(fmaf(l.x, back, h.x), fmaf(l.y, back, h.y));
 }
 
@@ -1140,7 +1151,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         float m_ref[R];
 #pragma unroll
         for (int n = 0; n < R; ++n) m_ref[n] = -CUDART_INF_F;
-        float l_acc = 0.f;                                // running sum of row r0 + my_row over the warp's keys
+        float l_thr[R];                                   // this thread's key: exact sums of p per row
+#pragma unroll
+        for (int n = 0; n < R; ++n) l_thr[n] = 0.f;
         float lt_acc[R];                                  // this thread's key: sums of p_hi + p_lo per row
 #pragma unroll
         for (int n = 0; n < R; ++n) lt_acc[n] = 0.f;
@@ -1214,13 +1227,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                     if (al != 1.f) moved |= 1u << n;
                     m_ref[n] = mn;
                 }
-                float a_mine = 1.f;
 #pragma unroll
-                for (int n = 0; n < R; ++n)
-                    if (n == my_row) a_mine = alpha[n];
-                l_acc *= a_mine;
-#pragma unroll
-                for (int n = 0; n < R; ++n) lt_acc[n] *= alpha[n];
+                for (int n = 0; n < R; ++n) {
+                    l_thr[n] *= alpha[n];
+                    lt_acc[n] *= alpha[n];
+                }
                 if (moved != 0 && blk > 0) {
                     // O^T holds blocks < blk: wait for the last P.V, then scale the
                     // columns (hi and lo, four d_v chunks) of the rows whose
@@ -1259,14 +1270,17 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             // set writes bytes [r0, r0 + R) of each half.
             if (blk >= 2) warp_wait(&ms.pv_done[st], ((blk - 2) >> 1) & 1, abort_flag);
             uint32_t hiw[R / 4], low[R / 4];
+            // the reference minus kShift, finite: a row whose reference is still
+            // -inf has seen no valid key, so all its logits are -inf too
+            float mfin[R];
+#pragma unroll
+            for (int n = 0; n < R; ++n)
+                mfin[n] = m_ref[n] == -CUDART_INF_F ? 0.f : m_ref[n] - kShift;
 #pragma unroll
             for (int n = 0; n < R; n += 4) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float x = s[n + u];
-                    s[n + u] = (x == -CUDART_INF_F || m_ref[n + u] == -CUDART_INF_F)
-                                   ? 0.f : ex2_approx(x - m_ref[n + u] + kShift);
-                }
+                for (int u = 0; u < 4; ++u)   // 2^-inf = 0 (mfin is finite)
+                    s[n + u] = ex2_approx(s[n + u] - mfin[n + u]);
                 uint16_t h0, l0, h1, l1;
                 const float2 t0 = split_pair<kPLoBits>(s[n], s[n + 1], h0, l0);
                 const float2 t1 = split_pair<kPLoBits>(s[n + 2], s[n + 3], h1, l1);
@@ -1274,6 +1288,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 lt_acc[n + 1] += t0.y;
                 lt_acc[n + 2] += t1.x;
                 lt_acc[n + 3] += t1.y;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) l_thr[n + u] += s[n + u];
                 hiw[n / 4] = (uint32_t)h0 | ((uint32_t)h1 << 16);
                 low[n / 4] = (uint32_t)l0 | ((uint32_t)l1 << 16);
             }
@@ -1293,12 +1309,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.p_full[st]);
             if (warp == kSoftmaxWarp0 && lane == 0) MLA_BLOCK_STAMP(blk, 4);
-            // Running sums of this warp's 32 keys (lane ends up with set row
-            // my_row).  The empty asm keeps the compiler from scheduling these
-            // shuffles ahead of the P hand-off above, where they would delay the MMA.
-#pragma unroll
-            for (int n = 0; n < R; ++n) asm volatile("" : "+f"(s[n]));
-            l_acc += warp_transpose_reduce<R, false>(s, lane);
         }
 
         // ---- epilogue ------------------------------------------------------------------------
@@ -1309,6 +1319,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         // a single split) into the idle KV stages, and one bulk TMA store per
         // row writes it out.  Each set handles its own rows.
         {
+            const float l_acc = warp_transpose_reduce<R, false>(l_thr, lane);
             const float t = warp_transpose_reduce<R, false>(lt_acc, lane);
             if ((lane % kLanesPerRow) == 0) {
                 red[sw * 32 + my_row] = l_acc;

@@ -119,10 +119,9 @@ typedef struct {
                                 their partials through each other's shared memory,
                                 the last cluster of a tile to finish merging the
                                 clusters' results; results do not depend on the
-                                timing.  The planner fuses only when one cluster
-                                holds all of a tile's splits; larger split counts
-                                may be fused by setting it (see
-                                mla_plan_force_splits) */
+                                timing.  The planner sets 1 (measured on GB300
+                                the fused merge never beat the reduce kernel);
+                                a caller may opt in by setting a size that fits */
 } mla_plan_t;
 
 /*
@@ -344,9 +343,8 @@ int mla_splitk_reduce(const float* o_part, const float* lse_part, int64_t rows,
 
 /*
  * Re-target a plan to a forced split count (1..MLA_MAX_SPLITS), updating its
- * grid, its merge cluster size (as the planner sets it: the fused merge when
- * num_splits is 2 or 4 and one cluster then holds all of a tile's splits,
- * else 1) and its workspace size.  For split sweeps
+ * grid, its merge cluster size (1, as the planner sets it) and its workspace
+ * size.  For split sweeps
  * (moonmath-ai/amd-kernels README, "Results -- MLA decode": num_kv_splits swept
  * per shape) and tests; the planner's own choice needs no call to it.  A
  * caller may set merge_cluster to 1 afterwards (the separate reduce) or to

@@ -22,14 +22,17 @@ inline int32_t rows_per_cta_for(int64_t rows) { return rows <= 16 ? 16 : 32; }
 
 // GB300 split rule (the wave-fill idea of hip_mha_decoding_num_partitions,
 // re-derived for this kernel: one resident CTA per SM, 128-key blocks).  A
-// small cost model in microseconds picks the split count: waves of CTAs times
-// (blocks per CTA x block time + per-CTA fixed time), plus the reduce (a launch
-// and the fp32 partial traffic) when there is more than one split.
-constexpr double kBlockUs = 1.65;      // 128 x 576 B at one SM's share of HBM bandwidth
-constexpr double kCtaUs = 2.0;         // prologue, pipeline fill, epilogue
-constexpr double kReduceUs = 2.0;      // reduce launch and its latency chain
-constexpr double kFusedUs = 0.6;       // fused merge: two cluster barriers and the slice merge
-constexpr double kTicketUs = 3.0;      // ... plus, with several clusters, ticket and L2 round trips
+// small cost model in microseconds picks the split count.  Each wave of CTAs
+// costs its blocks per CTA times the slower of the block's latency-bound time
+// and the wave's share of the GPU-wide gather rate, plus a fixed time per CTA;
+// several splits add the reduce (a launch and the fp32 partial traffic).  The
+// constants come from phase traces and split sweeps of this kernel on GB300.
+constexpr double kBlockUs16 = 1.6;     // a 128-key block, 16 query rows per CTA (latency-bound)
+constexpr double kBlockUs32 = 2.2;     // ... 32 query rows per CTA
+constexpr double kGather16 = 5.8e6;    // bytes/us gathered GPU-wide by 16-row CTAs
+constexpr double kGather32 = 4.4e6;    // ... by 32-row CTAs (a request's head blocks gather the same rows)
+constexpr double kCtaUs = 6.0;         // start-up to the first QK, and the epilogue
+constexpr double kReduceUs = 3.0;      // reduce launch and its latency chain
 constexpr double kBytesPerUs = 6.8e6;  // HBM bytes per microsecond
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -42,9 +45,6 @@ int64_t wave_ctas(int32_t sm_count, int32_t mc = 1)
 {
     return mc >= 4 ? (int64_t)sm_count - sm_count / 19 : sm_count;
 }
-
-// Merge cluster sizes the split kernel is built for, largest first.
-constexpr int32_t kMergeClusters[] = {4, 2};
 
 // Whether clusters of `mc` splits can fuse the merge of a plan: the split count
 // divides into clusters, every (tile, rank) has a ticket, and a CTA of the last
@@ -86,50 +86,51 @@ int64_t workspace_for(int64_t items, int ns, int d_v)
     return bytes;
 }
 
-// The merge cluster size the planner uses for a split count: the fused merge
-// when one cluster holds all of a tile's splits (ns of 2 or 4), else 1 (the
-// separate reduce).
-int32_t planned_merge_cluster(int64_t tiles, int32_t ns, int32_t rows_per_cta)
-{
-    for (int32_t mc : kMergeClusters)
-        if (ns == mc && fused_merge_ok(tiles, ns, rows_per_cta, mc)) return mc;
-    return 1;
-}
+// The merge cluster size the planner uses: 1, the separate reduce (see
+// gb300_splits); callers may opt into the fused merge by setting the plan's
+// merge_cluster to a size that fits.
+int32_t planned_merge_cluster(int64_t, int32_t, int32_t) { return 1; }
 
 struct SplitChoice {
     int32_t ns, mc;
 };
 
 // Split count and merge cluster size for `tiles` (request, head block) tiles
-// of `rows_per_cta` rows, `keys` keys per request and `items` output rows (row
-// x head) in the call: the cheapest by the cost model, over every split count
-// with the separate reduce and every fused-merge cluster size that fits.
+// of `rows_per_cta` rows, `keys` keys per request of `row_bytes`-byte rows and
+// `items` output rows (row x head) in the call: the cheapest by the cost
+// model, over every split count with the separate reduce and the fused merge
+// where one cluster holds a tile's splits.
 SplitChoice gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v,
-                         int32_t sm_count, int32_t rows_per_cta)
+                         int32_t row_bytes, int32_t sm_count, int32_t rows_per_cta)
 {
     const int64_t blocks = ceil_div(keys > 0 ? keys : 1, kBlockN);
-    const int64_t ctas = tiles > 0 ? tiles : 1;
+    const int64_t ctas1 = tiles > 0 ? tiles : 1;
     const int64_t max_ns = blocks < MLA_MAX_SPLITS ? blocks : MLA_MAX_SPLITS;
+    const double block_us = rows_per_cta == 16 ? kBlockUs16 : kBlockUs32;
+    const double us_per_cta_block = (double)kBlockN * row_bytes /
+                                    (rows_per_cta == 16 ? kGather16 : kGather32);
     double best = 0.0;
     SplitChoice pick{1, 1};
     auto consider = [&](int64_t ns, int32_t mc) {
-        const double waves = (double)ceil_div(ctas * ns, wave_ctas(sm_count, mc));
-        double t = waves * ((double)ceil_div(blocks, ns) * kBlockUs + kCtaUs);
+        const int64_t ctas = ctas1 * ns;
+        const int64_t wave = wave_ctas(sm_count, mc);
+        const double bpc = (double)ceil_div(blocks, ns);
+        auto wave_us = [&](int64_t active) {
+            const double b = (double)active * us_per_cta_block;
+            return bpc * (b > block_us ? b : block_us) + kCtaUs;
+        };
+        double t = (double)(ctas / wave) * wave_us(wave);
+        if (ctas % wave != 0) t += wave_us(ctas % wave);
         if (ns > 1 && mc == 1) t += kReduceUs + (double)items * ns * d_v * 4.0 * 2.0 / kBytesPerUs;
-        if (mc > 1) t += kFusedUs + (ns > mc ? kTicketUs : 0.0);
         if ((pick.ns == 1 && pick.mc == 1 && ns == 1) || t < best - 1e-9) {
             best = t;
             pick = SplitChoice{(int32_t)ns, mc};
         }
     };
-    for (int64_t ns = 1; ns <= max_ns; ++ns) {
-        consider(ns, 1);
-        // the fused merge only where one cluster holds every split of a tile:
-        // measured on GB300, a tile of several clusters (ticket, then a merge
-        // of the clusters' partials from L2) costs more than the reduce kernel
-        for (int32_t mc : kMergeClusters)
-            if (ns == mc && fused_merge_ok(ctas, (int32_t)ns, rows_per_cta, mc)) consider(ns, mc);
-    }
+    // The fused merge is not a candidate: measured on GB300 it never beat the
+    // reduce kernel (tiles of several clusters: c1 21.3 vs 19.5 us; one
+    // cluster per tile: B=1 S=256 11.4 vs 10.2 us, sparse 24 tokens equal).
+    for (int64_t ns = 1; ns <= max_ns; ++ns) consider(ns, 1);
     return pick;
 }
 
@@ -307,7 +308,7 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
     const int64_t head_blocks = ceil_div(rows, rows_per_cta_for(rows));
     const int64_t keys = batch > 0 ? ceil_div(total_keys, batch) : 0;
     const SplitChoice ch = gb300_splits(head_blocks * (batch > 0 ? batch : 1), keys,
-                                        (int64_t)batch * rows, d_v, sm_count,
+                                        (int64_t)batch * rows, d_v, d_v + d_rope, sm_count,
                                         rows_per_cta_for(rows));
     fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ch.ns, ch.mc);
     // Longest requests first once the grid outlasts one wave (variable lengths

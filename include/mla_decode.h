@@ -102,10 +102,9 @@ typedef struct {
     int64_t workspace_bytes; /* bytes of device workspace the call needs */
     int32_t batch, q_len, num_heads, d_v, d_rope, sm_count;
     int64_t total_keys;      /* dense: kv_indices length; sparse: tokens * (topk + extra_topk) */
-    int32_t kv_share;        /* head blocks (CTAs) that share each gathered KV block
-                                through a thread-block cluster and TMA multicast:
-                                1, 2, 4 or 8, dividing head_blocks (1 when
-                                rows_per_cta is 16); results do not depend on it */
+    int32_t kv_share;        /* 1: every CTA gathers its own KV rows (a request's
+                                head blocks read the same rows, the repeats
+                                served from L2); other values are rejected */
     int32_t extra_topk;      /* sparse: candidates per token in the second
                                 (compressed) cache, 0 without one; dense: 0 */
     int32_t long_first;      /* dense, 1: grid slice z serves the z-th longest
@@ -408,6 +407,22 @@ const char* mla_status_string(int status);
 int mla_debug_gather(const void* pool, int64_t pool_rows, int32_t row_bytes,
                      const int32_t* indices, int64_t n, void* out, void* workspace,
                      void* stream);
+
+/*
+ * Sets the bound, in SM clock cycles, of the split kernel's pipeline waits
+ * for launches enqueued after the call (process-wide; every device), and
+ * returns the previous bound; cycles <= 0 restores the default, about one
+ * second at GB300 clocks.  A wait that runs out ends its CTA's work: the CTA
+ * stops issuing copies and MMAs, waits (with the full bound) for those it
+ * already issued, writes what it has (its output rows are then unspecified),
+ * sets MLA_DEVERR_TIMEOUT in the workspace error word and exits; the call
+ * completes normally and the device stays usable.  For tests of that path:
+ * while a bound other than the default is set, every CTA also starts with a
+ * wait on a barrier that nothing completes, so at least that wait runs out
+ * while the CTA's first copies are in flight.  Not on the decode path; not
+ * thread-safe against concurrent decode calls that expect the default.
+ */
+int64_t mla_debug_wait_limit(int64_t cycles);
 
 /*
  * The split count that the wave-fill rule of hip_mha_decoding_num_partitions

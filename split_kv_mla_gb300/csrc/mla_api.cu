@@ -186,6 +186,13 @@ void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32
 
 }  // namespace
 
+// The bound of the split kernel's pipeline waits, in SM cycles (about a second
+// by default; mla_debug_wait_limit lowers it for tests of the timeout path).
+constexpr long long kDefaultWaitLimit = 2000000000ll;
+static std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+long long pipeline_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+bool stall_probe_armed() { return pipeline_wait_limit() != kDefaultWaitLimit; }
+
 // The workspace bytes a plan needs, from its shape and split count (the plan's
 // own workspace_bytes field is only a copy of this, and is checked against it).
 int64_t needed_workspace(const mla_plan_t* plan)
@@ -247,6 +254,8 @@ bool variant_ok(const mla_plan_t* plan)
 int run(const mla_plan_t* plan, SplitArgs& a, int64_t items, cudaStream_t stream,
         bool with_reduce)
 {
+    a.wait_limit = pipeline_wait_limit();
+    a.stall_probe = stall_probe_armed() ? 1 : 0;
     const int mc = with_reduce ? plan->merge_cluster : 1;
     a.tickets = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(a.err) + kErrorAreaBytes);
     cudaError_t e = launch_split_tc(a, *plan, mc, stream);
@@ -661,6 +670,12 @@ int mla_debug_gather(const void* pool, int64_t pool_rows, int32_t row_bytes,
                                         static_cast<uint32_t*>(workspace),
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH_FAILED;
+}
+
+int64_t mla_debug_wait_limit(int64_t cycles)
+{
+    const long long v = cycles > 0 ? (long long)cycles : kDefaultWaitLimit;
+    return (int64_t)g_wait_limit.exchange(v);
 }
 
 const char* mla_status_string(int status)

@@ -82,7 +82,18 @@ struct SplitArgs {
     uint32_t* tickets = nullptr;
     // phase time stamps (builds with MLA_TRACE only): kTraceSlots per CTA
     unsigned long long* trace = nullptr;
+    // cycle bound of the pipeline's waits (mla_debug_wait_limit; the waits that
+    // drain copies and MMAs before the CTA exits keep the full bound)
+    long long wait_limit = 2000000000ll;
+    // tests of the timeout path: the softmax warps first wait on a barrier that
+    // nothing completes, so that wait runs out while copies are in flight
+    int32_t stall_probe = 0;
 };
+
+// The pipeline wait bound that launches use (mla_debug_wait_limit sets it),
+// and whether that call armed the unsatisfiable wait of the timeout tests.
+long long pipeline_wait_limit();
+bool stall_probe_armed();
 
 // Phase stamps of a traced build (compiled with -DMLA_TRACE): per CTA of the
 // split kernel, globaltimer nanoseconds at kTraceSlots points, for at most

@@ -76,13 +76,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
 constexpr long long kWaitLimitCycles = 2000000000ll;
 
 // Wait for a phase, giving up (false) when *abort becomes nonzero or after
-// kWaitLimitCycles SM cycles; a timeout sets *abort so the CTA's other roles
-// stop too.  With sleep_ns > 0 the waiter backs off with nanosleep after a few
-// polls, leaving issue slots to the warps that share its SM sub-partition.
-// (The SM cycle counter bounds the wait: reading the global timer costs about a
-// microsecond.)
+// `limit` SM cycles (kWaitLimitCycles unless given); a timeout sets *abort so
+// the CTA's other roles stop too.  With sleep_ns > 0 the waiter backs off with
+// nanosleep after a few polls, leaving issue slots to the warps that share its
+// SM sub-partition.  (The SM cycle counter bounds the wait: reading the global
+// timer costs about a microsecond.)
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
-                                                   volatile int* abort, uint32_t sleep_ns = 0)
+                                                   volatile int* abort, uint32_t sleep_ns = 0,
+                                                   long long limit = kWaitLimitCycles)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
@@ -91,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
         if (sleep_ns != 0 && i > 4) __nanosleep(sleep_ns);
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort = 1;
                 return false;
             }

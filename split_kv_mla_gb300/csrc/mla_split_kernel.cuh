@@ -174,6 +174,8 @@ struct Cfg {
 
 struct Misc {
     uint64_t kv_full[2], kv_empty[2], pv_done[2], s_full[2], s_free[2], p_full[2], o_done;
+    uint64_t mma_drain;   // after an abort: every MMA the CTA issued has completed
+    uint64_t never;       // tests of the timeout path: a barrier nothing completes
     uint32_t tmem_base;
     int abort;
     int q3;   // some query row of the tile needs its third (q_lo) term
@@ -328,9 +330,10 @@ __device__ __forceinline__ bool softmax_bar_or(uint32_t id, bool v)
 // Bounded wait whose outcome is the same on every lane of the warp (all lanes
 // must call it), so no warp-collective instruction is reached divergently.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t sleep_ns = 0)
+                                          uint32_t sleep_ns = 0,
+                                          long long limit = kWaitLimitCycles)
 {
-    const bool ok = mbar_wait_or_abort(bar, parity, abort, sleep_ns);
+    const bool ok = mbar_wait_or_abort(bar, parity, abort, sleep_ns, limit);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -620,6 +623,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             mbar_init(&ms.p_full[i], 4 * kSets);
         }
         mbar_init(&ms.o_done, 1);
+        mbar_init(&ms.mma_drain, 1);
+        mbar_init(&ms.never, 1);
         ms.abort = 0;
         ms.q3 = 0;
         fence_mbar_init();
@@ -1004,7 +1009,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         // block j reuses the stage of block j-2: wait for its P.V, then load
         int issued = nblk < 2 ? nblk : 2;
         for (int j = 2; j < nblk; ++j) {
-            if (!warp_wait(&ms.kv_empty[j & 1], ((j - 2) >> 1) & 1, abort_flag, kGatherSleepNs))
+            if (!warp_wait(&ms.kv_empty[j & 1], ((j - 2) >> 1) & 1, abort_flag, kGatherSleepNs,
+                           a.wait_limit))
                 break;
             if (tid == 0) MLA_BLOCK_STAMP(j, 0);
             issue(j, fix_slots(gnext), row_valid(j, rnext));
@@ -1019,9 +1025,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 if (!pf_rows && j + 2 < nblk) lpf = pf_lines_load(j + 2);
             }
         }
-        // Never leave the CTA with loads in flight: the last two issued blocks
-        // (earlier ones were consumed before their stage was reused) must land.
-        // A fresh wait flag keeps this drain going even after an abort.
+        // Never leave the CTA with loads in flight: the last two blocks this
+        // warp issued (earlier ones were consumed before their stage was
+        // reused) must land.  A fresh wait flag and the full bound keep this
+        // drain going after an abort.  (After an abort another gather warp
+        // may have stopped one block earlier, leaving a phase that never
+        // completes; the wait then runs its full bound, about a second, long
+        // after this warp's own copies have landed.)
         volatile int drain_abort = 0;
         for (int j = issued - 2; j < issued; ++j)
             if (j >= 0) warp_wait(&ms.kv_full[j & 1], (j >> 1) & 1, &drain_abort, kGatherSleepNs);
@@ -1083,7 +1093,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             // softmax works on block j), P.V of the oldest block as soon as its
             // P is published (which frees the block's stage).  Both conditions
             // are polled without blocking; P.V goes first when both are ready.
-            // No progress for kWaitLimitCycles ends the loop with the abort flag.
+            // No progress for a.wait_limit cycles ends the loop with the abort flag.
             int next_qk = 0, next_pv = 0;
             long long t_last = clock64();
             // a poll's outcome comes from lane 0, so every lane takes the same path
@@ -1121,11 +1131,19 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                     const long long now = clock64();
                     if (*abort_flag) break;
                     if (idle == 64) t_last = now;   // first check of this idle stretch
-                    else if (now - t_last > kWaitLimitCycles) {
+                    else if (now - t_last > a.wait_limit) {
                         *abort_flag = 1;
                         break;
                     }
                 }
+            }
+            // After an abort, MMAs already issued may still be running: wait
+            // for them (with the full bound) before the CTA releases TMEM and
+            // its stages.  Without one, o_done has already covered them.
+            if (__shfl_sync(0xffffffffu, *abort_flag != 0 ? 1 : 0, 0) != 0) {
+                umma_commit_warp(&ms.mma_drain);
+                volatile int drain_abort = 0;
+                warp_wait(&ms.mma_drain, 0, &drain_abort);
             }
         }
         __syncwarp();
@@ -1158,11 +1176,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
         for (int n = 0; n < R; ++n) lt_acc[n] = 0.f;
         bool alive = true;
+        // tests of the timeout path: a wait that nothing ends runs out (and
+        // sets the abort flag) while the CTA's first copies are in flight
+        if (a.stall_probe && nblk > 0) warp_wait(&ms.never, 0, abort_flag, 0, a.wait_limit);
         for (int blk = 0; blk < nblk; ++blk) {
             const int st = blk & 1;
             const uint32_t ph = (blk >> 1) & 1;
-            bool ok = warp_wait(&ms.kv_full[st], ph, abort_flag) &&
-                      warp_wait(&ms.s_full[st], ph, abort_flag);
+            bool ok = warp_wait(&ms.kv_full[st], ph, abort_flag, 0, a.wait_limit) &&
+                      warp_wait(&ms.s_full[st], ph, abort_flag, 0, a.wait_limit);
             float s[R];
             if (ok) {
                 tc_fence_after();
@@ -1236,7 +1257,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                     // O^T holds blocks < blk: wait for the last P.V, then scale the
                     // columns (hi and lo, four d_v chunks) of the rows whose
                     // reference moved; the loop over rows is uniform.
-                    if (warp_wait(&ms.pv_done[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag)) {
+                    if (warp_wait(&ms.pv_done[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag, 0,
+                                  a.wait_limit)) {
                         tc_fence_after();
 #pragma unroll 1
                         while (moved != 0) {
@@ -1268,7 +1290,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
             // P^T row ti: bytes [0, N) = p_hi, [N, 2N) = p_lo, of p * 2^kShift; this
             // set writes bytes [r0, r0 + R) of each half.
-            if (blk >= 2) warp_wait(&ms.pv_done[st], ((blk - 2) >> 1) & 1, abort_flag);
+            if (blk >= 2) warp_wait(&ms.pv_done[st], ((blk - 2) >> 1) & 1, abort_flag, 0, a.wait_limit);
             uint32_t hiw[R / 4], low[R / 4];
             // the reference minus kShift, finite: a row whose reference is still
             // -inf has seen no valid key, so all its logits are -inf too
@@ -1341,7 +1363,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 ? ((int64_t)b * a.q_len + idx / a.num_heads) * a.num_heads + idx % a.num_heads
                 : -1;
         }
-        const bool have_o = alive && nblk > 0 && warp_wait(&ms.o_done, 0, abort_flag);
+        const bool have_o = alive && nblk > 0 && warp_wait(&ms.o_done, 0, abort_flag, 0, a.wait_limit);
         if (warp == kSoftmaxWarp0 && lane == 0) MLA_STAMP(5);
         if (have_o) tc_fence_after();
         softmax_bar(bar_id);

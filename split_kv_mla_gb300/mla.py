@@ -104,6 +104,7 @@ def load(build_if_missing: bool = True, path: Optional[str] = None):
             "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "mla_wave_fill_splits": (i32, [i32, i64, i32, i32, i32, i32, i32, i32, i32]),
             "mla_debug_gather": (ctypes.c_int, [vp, i64, i32, vp, i64, vp, vp, vp]),
+            "mla_debug_wait_limit": (i64, [i64]),
             "mla_decode_dcp": (ctypes.c_int, [P, vp, vp, vp, i64, vp, vp, vp, i32, i32, i32,
                                               f32, f32, vp, i32, i32, i32, vp, vp, vp, i64,
                                               vp]),
@@ -439,6 +440,13 @@ def mla_debug_gather(pool, indices, workspace_t=None, stream=None):
                                    _dev_ptr(out, "out"), _dev_ptr(ws, "workspace"),
                                    _stream_ptr(stream)), "mla_debug_gather")
     return out, ws
+
+
+def mla_debug_wait_limit(cycles: int) -> int:
+    """Set the bound (SM cycles) of the split kernel's pipeline waits for later
+    launches; <= 0 restores the default.  Returns the previous bound.  For tests
+    of the timeout path."""
+    return int(load().mla_debug_wait_limit(int(cycles)))
 
 
 def mla_decode_noalloc(plan: mla_plan_t, q_lat, q_pe, pool, seq_lens, kv_indices, kv_indptr,

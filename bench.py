@@ -743,7 +743,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (round(value / pages_baseline_gbs(args.workload), 3)
                         if pages_baseline_gbs(args.workload) else None),
-        "dtype": "e4m3fn-kv/bf16-q/fp32-acc",
+        "dtype": "e4m3fn-kv/bf16-q(e4m3 hi+mid[+lo])/p(e4m3 hi+lo)/fp32-acc",
         "data": "synthetic (seeded; N(0,1) bf16 queries, N(0,1)/kv_scale e4m3fn pool, shuffled page_size-1 slots)",
         "config": {"workload": f"{args.workload}: dense MLA decode {desc}" if dense
                    else f"{args.workload}: sparse top-k MLA decode {desc}",

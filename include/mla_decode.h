@@ -374,7 +374,8 @@ int mla_read_device_error(const void* workspace, int32_t* code, void* stream);
  *     MLA_ERR_WORKSPACE_TOO_SMALL and nothing is enqueued.
  *   - Set-up: the first call on a device (with that device current) looks up
  *     the array's device address once; make that first call before any stream
- *     capture on the device.
+ *     capture on the device.  The address is kept for the life of the process,
+ *     so do not use this entry point on a device after cudaDeviceReset.
  *   - Every call shares the one array and it keeps the last call's contents, so
  *     calls that overlap on the GPU (on different streams, or from different
  *     threads) race and must be serialised by the caller.

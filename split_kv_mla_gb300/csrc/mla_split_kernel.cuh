@@ -264,16 +264,19 @@ __device__ __forceinline__ float2 split_pair(float a, float b, uint16_t& hi, uin
 // Split two fp32 values of a scaled query row (max |x| < 256) into three e4m3
 // terms, x = hi + 2^-5 (mid + 2^-5 lo), bytes packed lo-byte first.  Exact for
 // every element of at least 2^-12 (the residuals are formed exactly in fp32).
-__device__ __forceinline__ void split_q3(float a, float b, uint16_t& hi, uint16_t& mid,
-                                         uint16_t& lo)
+// Returns |lo| of the two values (before lo is rounded to e4m3).
+__device__ __forceinline__ float split_q3(float a, float b, uint16_t& hi, uint16_t& mid,
+                                          uint16_t& lo)
 {
     constexpr float up = (float)(1 << kQLoBits);
     hi = f32x2_to_e4m3x2(a, b);
-    const float2 h = e4m3x2_to_f32x2((uint32_t)hi);
+    const float2 h = e4m3x2_to_f32x2_cvt(hi);
     const float ra = (a - h.x) * up, rb = (b - h.y) * up;
     mid = f32x2_to_e4m3x2(ra, rb);
-    const float2 m = e4m3x2_to_f32x2((uint32_t)mid);
-    lo = f32x2_to_e4m3x2((ra - m.x) * up, (rb - m.y) * up);
+    const float2 m = e4m3x2_to_f32x2_cvt(mid);
+    const float la = (ra - m.x) * up, lb = (rb - m.y) * up;
+    lo = f32x2_to_e4m3x2(la, lb);
+    return fabsf(la) + fabsf(lb);   // the two lo terms' size, before their rounding
 }
 
 // Reduce N values held by every lane of a warp (max or sum); afterwards lane l
@@ -960,15 +963,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     uint16_t h0, m0, l0, h1, m1, l1;
-                    split_q3(mul_pow2(__uint_as_float(w[2 * k] << 16), sh),
-                             mul_pow2(__uint_as_float(w[2 * k] & 0xFFFF0000u), sh), h0, m0, l0);
-                    split_q3(mul_pow2(__uint_as_float(w[2 * k + 1] << 16), sh),
-                             mul_pow2(__uint_as_float(w[2 * k + 1] & 0xFFFF0000u), sh), h1, m1, l1);
+                    lsum += split_q3(mul_pow2(__uint_as_float(w[2 * k] << 16), sh),
+                                     mul_pow2(__uint_as_float(w[2 * k] & 0xFFFF0000u), sh), h0, m0, l0);
+                    lsum += split_q3(mul_pow2(__uint_as_float(w[2 * k + 1] << 16), sh),
+                                     mul_pow2(__uint_as_float(w[2 * k + 1] & 0xFFFF0000u), sh), h1, m1, l1);
                     hw[k] = (uint32_t)h0 | ((uint32_t)h1 << 16);
                     mw[k] = (uint32_t)m0 | ((uint32_t)m1 << 16);
                     lw[k] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-                    const float2 la = e4m3x2_to_f32x2(l0), lb = e4m3x2_to_f32x2(l1);
-                    lsum += (fabsf(la.x) + fabsf(la.y)) + (fabsf(lb.x) + fabsf(lb.y));
                 }
                 *reinterpret_cast<uint2*>(qtile + tile_offset(n, c, NQ)) = make_uint2(hw[0], hw[1]);
                 *reinterpret_cast<uint2*>(qtile + tile_offset(N + n, c, NQ)) = make_uint2(mw[0], mw[1]);

@@ -107,7 +107,8 @@ __device__ __forceinline__ void trace_block(const SplitArgs& a, int j, int e)
 // published, 5 P.V issued.
 // Stamp slots: 0 CTA start, 1 after the wait for the preceding kernel,
 // 2 first gather issued, 3 first QK issued, 4 last P.V issued, 5 epilogue has
-// O, 6 rows staged, 7 rows stored, 8 end.
+// O, 6 rows staged, 7 rows stored, 8 end, 9 query tile written (first query
+// warp), 10 the MMA warp past the query tile's barrier.
 
 
 using namespace sm100;
@@ -991,10 +992,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 if (lsum * (448.f / 1024.f) * fabsf(cq) > 1.f / 65536.f) ms.q3 = 1;
             }
         }
+        if (warp == kSoftmaxWarp0 && lane == 0) MLA_STAMP(9);
     }
     if (warp >= kMmaWarp) {   // the query warps and the MMA warp, which waits for the tile
         fence_proxy_async_smem();
         asm volatile("bar.sync %0, %1;" ::"n"(kQBar), "n"((kQWarps + 1) * 32) : "memory");
+        if (warp == kMmaWarp && lane == 0) MLA_STAMP(10);
     }
     // QK runs over 3N columns (hi, mid, lo) when some row needs its q_lo term,
     // else over the first 2N; the MMA warp and the softmax warps read the

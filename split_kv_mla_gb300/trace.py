@@ -29,7 +29,8 @@ MAX_CTAS = 8192     # kTraceCtas
 BLOCK_CTAS, BLOCKS, BLOCK_EVENTS = 4, 64, 6   # per-block events of the first CTAs
 WORDS = MAX_CTAS * SLOTS + BLOCK_CTAS * BLOCKS * BLOCK_EVENTS
 EVENTS = ["issue", "issued", "qk", "s_read", "p_done", "pv"]
-PHASES = ["start", "waited", "gather0", "qk0", "pv_last", "o_ready", "staged", "stored", "end"]
+PHASES = ["start", "waited", "gather0", "qk0", "pv_last", "o_ready", "staged", "stored", "end",
+          "q_tile", "mma_go"]
 
 
 def build_traced() -> str:

@@ -776,7 +776,9 @@ def run_ours(args, rank, world, local_rank):
     oracle_here = not args.no_cpu_baseline and rank == 0 and world == 1
     if oracle_here:
         out["cpu_baseline"] = cpu_baseline(kind, inp, args.cpu_budget)
-    if args.workloads != "none":
+    # every workload in single-GPU runs (multi-rank runs time the headline only,
+    # unless a list is given)
+    if args.workloads != "none" and not (args.workloads == "all" and world > 1):
         names = ALL_WORKLOADS if args.workloads == "all" else args.workloads.split(",")
         del runner
         torch.cuda.empty_cache()
@@ -872,8 +874,8 @@ def main(argv=None):
     ap.add_argument("--splits", type=int, default=0,
                     help="force the split count instead of the planner's (split sweeps)")
     ap.add_argument("--workloads", default="all",
-                    help="also time these workloads in the same run: all, none, or a "
-                         "comma-separated list")
+                    help="also time these workloads in the same run: all (single-GPU "
+                         "runs), none, or a comma-separated list")
     ap.add_argument("--workload-steps", type=int, default=200)
     ap.add_argument("--workload-cpu-budget", type=float, default=1.5)
     args = ap.parse_args(argv)

@@ -27,10 +27,11 @@ inline int32_t rows_per_cta_for(int64_t rows) { return rows <= 16 ? 16 : 32; }
 // and the wave's share of the GPU-wide gather rate, plus a fixed time per CTA;
 // several splits add the reduce (a launch and the fp32 partial traffic).  The
 // constants come from phase traces and split sweeps of this kernel on GB300.
-constexpr double kBlockUs16 = 1.6;     // a 128-key block, 16 query rows per CTA (latency-bound)
+constexpr double kBlockUs16 = 2.1;     // a 128-key block, 16 query rows per CTA (latency-bound)
 constexpr double kBlockUs32 = 2.2;     // ... 32 query rows per CTA
-constexpr double kGather16 = 5.8e6;    // bytes/us gathered GPU-wide by 16-row CTAs
-constexpr double kGather32 = 4.4e6;    // ... by 32-row CTAs (a request's head blocks gather the same rows)
+constexpr double kGather32 = 4.4e6;    // bytes/us gathered GPU-wide by 32-row CTAs (a
+                                       // request's head blocks gather the same rows); 16-row
+                                       // CTAs measured no GPU-wide cap up to a full wave
 constexpr double kCtaUs = 6.0;         // start-up to the first QK, and the epilogue
 constexpr double kReduceUs = 3.0;      // reduce launch and its latency chain
 constexpr double kBytesPerUs = 6.8e6;  // HBM bytes per microsecond
@@ -107,8 +108,8 @@ SplitChoice gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v
     const int64_t ctas1 = tiles > 0 ? tiles : 1;
     const int64_t max_ns = blocks < MLA_MAX_SPLITS ? blocks : MLA_MAX_SPLITS;
     const double block_us = rows_per_cta == 16 ? kBlockUs16 : kBlockUs32;
-    const double us_per_cta_block = (double)kBlockN * row_bytes /
-                                    (rows_per_cta == 16 ? kGather16 : kGather32);
+    const double us_per_cta_block =
+        rows_per_cta == 16 ? 0.0 : (double)kBlockN * row_bytes / kGather32;
     double best = 0.0;
     SplitChoice pick{1, 1};
     auto consider = [&](int64_t ns, int32_t mc) {

@@ -234,6 +234,10 @@ def test_long_first_only_when_the_grid_outlasts_a_wave():
     (2, 1, 64, 65536, 37),      # c2 2x65536
     (16, 1, 64, 131072, 9),     # c2 16x131072
     (64, 1, 128, 16896, 1),     # c3's shape (mean length)
+    (8, 1, 16, 131072, 19),     # longer H=16 contexts: a full wave
+    (8, 1, 16, 65536, 19),
+    (16, 1, 16, 131072, 19),
+    (64, 1, 16, 16384, 2),
 ])
 def test_dense_plan_stays_within_the_measured_best(batch, q_len, heads, keys_per_request,
                                                    splits):

@@ -803,20 +803,28 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (!(SPARSE && v < 0)) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
         return 0;
     };
-    // Block j into stage j & 1.  Warp 0 announces the whole stage's bytes, which
-    // arrive from the seven warps' copies.
+    // Block j into stage j & 1.  Warp 0 announces the stage's bytes, which
+    // arrive from the seven warps' copies.  The four-row groups past the split's
+    // end are not fetched from block 2 on: their rows are masked, and the stage
+    // still holds block j-2's rows there (finite bytes; the copy engine's issue
+    // rate, not DRAM, bounds a block, so a short last block costs less).  The
+    // stages' first fills copy every group (row 0 for masked rows), so no row of
+    // a stage is ever read uninitialised.
     auto issue = [&](int j, const Slots& sl, int rowok) {
         const int st = j & 1;
+        const int nk = min(kBlockN, k1 - (k0 + j * kBlockN));
+        const int ngrp = j >= 2 ? (nk + 3) >> 2 : kBlockN / 4;
         if (row_lane) ms.kvalid[st][tid] = rowok;
         __syncwarp();
         if (lane == 0) {
             if (warp == 0)
-                mbar_arrive_expect_tx(&ms.kv_full[st], (uint32_t)C::kStageBytes);
+                mbar_arrive_expect_tx(&ms.kv_full[st],
+                                      (uint32_t)(ngrp * (C::kStageBytes / (kBlockN / 4))));
             else
                 mbar_arrive(&ms.kv_full[st]);
         }
         __syncwarp();
-        if (item_on) {
+        if (item_on && my_group < ngrp) {
             uint8_t* stage = smem + C::kOffStage + st * C::kStageBytes;
             uint8_t* dst = my_box < 4 ? stage + my_box * C::kLatChunkBytes + my_group * 512
                                       : stage + 4 * C::kLatChunkBytes + my_group * 256;

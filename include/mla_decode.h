@@ -92,7 +92,11 @@ extern "C" {
  */
 typedef struct {
     int32_t num_splits;      /* KV ranges per request (1..MLA_MAX_SPLITS) */
-    int32_t rows_per_cta;    /* query rows (draft position x head) per CTA */
+    int32_t rows_per_cta;    /* query rows (draft position x head) per CTA: 16, or 32
+                                when a request has more than 16 rows; above 16 the
+                                planners take 16 where a CTA's work is short (a
+                                32-row CTA starts later), else 32; results agree
+                                with the oracle either way */
     int32_t block_n;         /* keys per pipeline block */
     int32_t head_blocks;     /* CTAs sharing one (request, split) */
     int32_t grid_x, grid_y, grid_z;  /* head_blocks, num_splits, batch (or tokens) */

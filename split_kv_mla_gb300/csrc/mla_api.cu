@@ -15,10 +15,17 @@ constexpr int kMaxHeads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Split-kernel geometry: 128 keys per block; 16 query rows per CTA when a
-// request has at most 16 (heads x draft positions), else 32.
+// request has at most 16 (heads x draft positions); above that 32, or 16 where
+// the planners find the smaller tile faster (short work per CTA, below).
 constexpr int kBlockN = 128;
 
 inline int32_t rows_per_cta_for(int64_t rows) { return rows <= 16 ? 16 : 32; }
+
+// A plan's rows per CTA: 16 for any row count, 32 only above 16 rows.
+inline bool rows_per_cta_ok(int64_t rows, int32_t rpc)
+{
+    return rpc == 16 || (rpc == 32 && rows > 16);
+}
 
 // GB300 split rule (the wave-fill idea of hip_mha_decoding_num_partitions,
 // re-derived for this kernel: one resident CTA per SM, 128-key blocks).  A
@@ -33,6 +40,10 @@ constexpr double kGather32 = 4.4e6;    // bytes/us gathered GPU-wide by 32-row C
                                        // request's head blocks gather the same rows); 16-row
                                        // CTAs measured no GPU-wide cap up to a full wave
 constexpr double kCtaUs = 6.0;         // start-up to the first QK, and the epilogue
+constexpr double kFirstBlockUs32 = 5.0;  // a 32-row CTA's extra start-up over a 16-row one
+                                         // (its query tile and first softmax): CTAs of one
+                                         // block took 4.9-5.2 us longer at 32 rows than at
+                                         // 16 (H=64, S=256..4096)
 constexpr double kReduceUs = 3.0;      // reduce launch and its latency chain
 constexpr double kBytesPerUs = 6.8e6;  // HBM bytes per microsecond
 
@@ -94,6 +105,7 @@ int32_t planned_merge_cluster(int64_t, int32_t, int32_t) { return 1; }
 
 struct SplitChoice {
     int32_t ns, mc;
+    double us;   // the cost model's time of the call
 };
 
 // Split count and merge cluster size for `tiles` (request, head block) tiles
@@ -111,7 +123,7 @@ SplitChoice gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v
     const double us_per_cta_block =
         rows_per_cta == 16 ? 0.0 : (double)kBlockN * row_bytes / kGather32;
     double best = 0.0;
-    SplitChoice pick{1, 1};
+    SplitChoice pick{1, 1, 0.0};
     auto consider = [&](int64_t ns, int32_t mc) {
         const int64_t ctas = ctas1 * ns;
         const int64_t wave = wave_ctas(sm_count, mc);
@@ -125,7 +137,7 @@ SplitChoice gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v
         if (ns > 1 && mc == 1) t += kReduceUs + (double)items * ns * d_v * 4.0 * 2.0 / kBytesPerUs;
         if ((pick.ns == 1 && pick.mc == 1 && ns == 1) || t < best - 1e-9) {
             best = t;
-            pick = SplitChoice{(int32_t)ns, mc};
+            pick = SplitChoice{(int32_t)ns, mc, t};
         }
     };
     // The fused merge is not a candidate: measured on GB300 it never beat the
@@ -161,12 +173,13 @@ int32_t sparse_splits(int64_t ctas, int64_t topk, int32_t sm_count)
 }
 
 void fill_plan(mla_plan_t* p, int32_t batch, int32_t q_len, int32_t heads, int32_t d_v,
-               int32_t d_rope, int32_t sm_count, int64_t total_keys, int32_t ns, int32_t mc)
+               int32_t d_rope, int32_t sm_count, int64_t total_keys, int32_t ns, int32_t mc,
+               int32_t rpc)
 {
     const int32_t rows = q_len * heads;
     std::memset(p, 0, sizeof *p);
     p->num_splits = ns;
-    p->rows_per_cta = rows_per_cta_for(rows);
+    p->rows_per_cta = rpc;
     p->block_n = kBlockN;
     p->head_blocks = (int32_t)ceil_div(rows, p->rows_per_cta);
     p->grid_x = p->head_blocks;
@@ -235,7 +248,7 @@ bool variant_ok(const mla_plan_t* plan)
     if (plan->q_len < 1 || plan->num_heads < 1 || plan->batch < 0) return false;
     const int64_t rows = (int64_t)plan->q_len * plan->num_heads;
     if (rows > (1 << 20)) return false;
-    if (plan->rows_per_cta != rows_per_cta_for(rows) || plan->block_n != kBlockN ||
+    if (!rows_per_cta_ok(rows, plan->rows_per_cta) || plan->block_n != kBlockN ||
         plan->head_blocks != ceil_div(rows, plan->rows_per_cta) ||
         plan->grid_x != plan->head_blocks || plan->grid_y != plan->num_splits ||
         plan->grid_z != plan->batch)
@@ -315,12 +328,25 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
         return MLA_ERR_UNSUPPORTED_SHAPE;
     const int64_t rows = (int64_t)q_len * num_heads;
     if (rows > (1 << 20)) return MLA_ERR_UNSUPPORTED_SHAPE;
-    const int64_t head_blocks = ceil_div(rows, rows_per_cta_for(rows));
     const int64_t keys = batch > 0 ? ceil_div(total_keys, batch) : 0;
-    const SplitChoice ch = gb300_splits(head_blocks * (batch > 0 ? batch : 1), keys,
-                                        (int64_t)batch * rows, d_v, d_v + d_rope, sm_count,
-                                        rows_per_cta_for(rows));
-    fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ch.ns, ch.mc);
+    auto choose = [&](int32_t rpc) {
+        return gb300_splits(ceil_div(rows, rpc) * (batch > 0 ? batch : 1), keys,
+                            (int64_t)batch * rows, d_v, d_v + d_rope, sm_count, rpc);
+    };
+    // Above 16 rows, the 32-row tile against the 16-row one (twice the head
+    // blocks, each gathering the same rows): the smaller tile wins where a
+    // CTA's work is short, since a 32-row CTA starts about 5 us later.
+    int32_t rpc = rows_per_cta_for(rows);
+    SplitChoice ch = choose(rpc);
+    if (rpc == 32) {
+        const SplitChoice ch16 = choose(16);
+        if (ch16.us < ch.us + kFirstBlockUs32) {
+            rpc = 16;
+            ch = ch16;
+        }
+    }
+    fill_plan(out, batch, q_len, num_heads, d_v, d_rope, sm_count, total_keys, ch.ns, ch.mc,
+              rpc);
     // Longest requests first once the grid outlasts one wave (variable lengths
     // then leave the short requests for the last wave).
     const int64_t ctas = (int64_t)out->grid_x * out->grid_y * out->grid_z;
@@ -340,14 +366,27 @@ int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
         return MLA_ERR_UNSUPPORTED_SHAPE;
     const int32_t cap = max_splits == 0 ? MLA_MAX_SPLITS
                                         : (max_splits < MLA_MAX_SPLITS ? max_splits : MLA_MAX_SPLITS);
-    const int64_t head_blocks = ceil_div(num_heads, rows_per_cta_for(num_heads));
-    int32_t ns = sparse_splits(head_blocks * (num_tokens > 0 ? num_tokens : 1),
-                               (int64_t)topk + extra_topk, sm_count);
-    if (ns > cap) ns = cap;
-    const int32_t rpc = rows_per_cta_for(num_heads);
+    const int64_t keys = (int64_t)topk + extra_topk;
+    auto splits_for = [&](int32_t rpc) {
+        const int32_t ns = sparse_splits(ceil_div(num_heads, rpc) * (num_tokens > 0 ? num_tokens : 1),
+                                         keys, sm_count);
+        return ns > cap ? cap : ns;
+    };
+    // Above 16 heads, 16-row CTAs (twice the head blocks) where the 32-row
+    // split would leave each CTA at most two 128-key blocks: a 32-row CTA
+    // starts about 5 us later, which short work cannot amortise.  Measured on
+    // GB300 (64 heads, top-k 2048): T=1 14.1 -> 10.5 us, T=4 16.4 -> 11.6, T=8
+    // 16.4 -> 15.5; at T=16 (four blocks per 32-row CTA) 32 rows stay faster.
+    int32_t rpc = rows_per_cta_for(num_heads);
+    int32_t ns = splits_for(rpc);
+    if (rpc == 32 && ceil_div(ceil_div(keys > 0 ? keys : 1, ns), kBlockN) <= 2) {
+        rpc = 16;
+        ns = splits_for(16);
+    }
+    const int64_t head_blocks = ceil_div(num_heads, rpc);
     fill_plan(out, num_tokens, 1, num_heads, d_v, d_rope, sm_count,
-              (int64_t)num_tokens * ((int64_t)topk + extra_topk), ns,
-              planned_merge_cluster(head_blocks * num_tokens, ns, rpc));
+              (int64_t)num_tokens * keys, ns,
+              planned_merge_cluster(head_blocks * num_tokens, ns, rpc), rpc);
     out->extra_topk = extra_topk;
     return MLA_OK;
 }

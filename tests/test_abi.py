@@ -197,10 +197,11 @@ def test_decode_rejects_a_plan_whose_fields_disagree(lib):
     # the kernels index the workspace and outputs by the plan's geometry, so a
     # plan edited out of step with its shape is refused before any launch
     base = mla.mla_plan_force_splits(mla.mla_decode_plan(2, 1, 64, 8192, 152), 4)
+    other_tile = 32 if base.rows_per_cta == 16 else 16
     edits = [("workspace_bytes", base.workspace_bytes - 256),      # stale size
              ("workspace_bytes", base.workspace_bytes + 256),
              ("grid_y", 5), ("grid_x", 1), ("grid_z", 3), ("head_blocks", 1),
-             ("rows_per_cta", 16), ("block_n", 64)]
+             ("rows_per_cta", other_tile), ("rows_per_cta", 8), ("block_n", 64)]
     for field, value in edits:
         q = mla.mla_plan_t.from_buffer_copy(base)
         setattr(q, field, value)
@@ -210,11 +211,41 @@ def test_decode_rejects_a_plan_whose_fields_disagree(lib):
     assert _call_decode(lib, base, ws_bytes=1 << 30, batch=2, heads=64) not in (-1, -3, -4)
 
 
-@pytest.mark.parametrize("tokens,splits", [(1, 16), (8, 8), (24, 2), (64, 1)])
-def test_sparse_plan_matches_the_measured_best_split(tokens, splits):
-    # 64 heads, top-k 2048, 152 SMs: the split counts a forced-split sweep of the
-    # sparse workload measured fastest on GB300 (the c4 token counts)
-    assert mla.mla_sparse_decode_plan(tokens, 64, 2048, 152).num_splits == splits
+@pytest.mark.parametrize("tokens,rows_per_cta,splits", [
+    (1, 16, 16), (2, 16, 16), (4, 16, 8), (8, 16, 4), (16, 32, 4), (24, 32, 2), (64, 32, 1)])
+def test_sparse_plan_matches_the_measured_best_tile_and_split(tokens, rows_per_cta, splits):
+    # 64 heads, top-k 2048, 152 SMs: the tile and split count that forced sweeps
+    # of the sparse workload measured fastest (or within 3 %) on GB300
+    p = mla.mla_sparse_decode_plan(tokens, 64, 2048, 152)
+    assert (p.rows_per_cta, p.num_splits) == (rows_per_cta, splits)
+    assert p.head_blocks == 64 // rows_per_cta
+
+
+@pytest.mark.parametrize("batch,q_len,heads,keys_per_request,rows_per_cta", [
+    (1, 1, 64, 256, 16), (1, 1, 64, 1024, 16), (1, 1, 64, 4096, 16), (2, 1, 64, 2048, 16),
+    (4, 1, 64, 1024, 16), (1, 1, 32, 2048, 16), (1, 4, 16, 8192, 16), (2, 1, 128, 1024, 16),
+    (8, 4, 16, 8192, 32), (1, 1, 64, 131072, 32), (2, 1, 64, 65536, 32),
+    (8, 1, 64, 131072, 32), (64, 1, 128, 16896, 32), (8, 1, 16, 8192, 16)])
+def test_dense_tile_follows_the_measured_best(batch, q_len, heads, keys_per_request,
+                                              rows_per_cta):
+    # Above 16 rows the planner weighs 16-row tiles (twice the head blocks)
+    # against 32-row ones; a forced sweep on GB300 measured these shapes
+    # fastest at the given tile (the small ones 25-35 % faster at 16 rows)
+    p = mla.mla_decode_plan(batch, q_len, heads, batch * keys_per_request, 152)
+    assert p.rows_per_cta == rows_per_cta
+    assert p.head_blocks == -(-(q_len * heads) // rows_per_cta)
+
+
+def test_plans_may_carry_either_tile_above_16_rows(lib):
+    # a 64-head plan is accepted with 16 or 32 rows per CTA (geometry in step);
+    # 32 rows for a request of at most 16 rows is refused
+    for rpc in (16, 32):
+        q = mla.mla_plan_force_splits(mla.mla_decode_plan(2, 1, 64, 8192, 152), 4)
+        q.rows_per_cta, q.head_blocks, q.grid_x = rpc, 64 // rpc, 64 // rpc
+        assert _call_decode(lib, q, ws_bytes=1 << 30, batch=2, heads=64) not in (-1, -3, -4)
+    q = mla.mla_decode_plan(2, 1, 16, 8192, 152)
+    q.rows_per_cta = 32
+    assert _call_decode(lib, q, ws_bytes=1 << 30, batch=2, heads=16) == -1
 
 
 def test_long_first_only_when_the_grid_outlasts_a_wave():

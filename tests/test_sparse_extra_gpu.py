@@ -93,13 +93,21 @@ def test_token_with_no_valid_candidate():
     compare(o, lse, ro, rl, "empty token")
 
 
-def test_second_cache_on_four_head_blocks():
-    # H=128: four 32-row head blocks, each gathering its own rows of both caches
+@pytest.mark.parametrize("rows_per_cta", [32, 16])
+def test_second_cache_on_several_head_blocks(rows_per_cta):
+    # H=128: four 32-row or eight 16-row head blocks, each gathering its own
+    # rows of both caches
     inp = gen.sparse_extra_inputs(4, 128, 1024, 256, 8192, 2048, seed=3)
-    o, lse, plan = _run(inp)
-    assert plan.head_blocks == 4
+    plan = mla.mla_sparse_decode_plan(4, 128, 1024, mla.sm_count(), extra_topk=256)
+    plan.rows_per_cta = rows_per_cta
+    plan.head_blocks = plan.grid_x = 128 // rows_per_cta
+    o, lse = mla.mla_sparse_decode_extra(plan, inp.q_nope.cuda(), inp.q_pe.cuda(),
+                                         inp.pool.cuda(), inp.indices.cuda(),
+                                         inp.extra_pool.cuda(), inp.extra_indices.cuda(),
+                                         inp.scale, inp.kv_scale)
+    torch.cuda.synchronize()
     ro, rl = oracle.sparse_extra_decode(inp)
-    compare(o, lse, ro, rl, "H=128 second cache")
+    compare(o, lse, ro, rl, f"H=128 second cache, {rows_per_cta} rows per CTA")
 
 
 def test_out_of_range_second_cache_slot_sets_error_word():

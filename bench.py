@@ -251,12 +251,13 @@ def recorded_traffic(workload: str):
 class Runner:
     """Device copies of one workload and the calls that run it."""
 
-    def __init__(self, kind, inp, device, copies, force_splits=0):
+    def __init__(self, kind, inp, device, copies, force_splits=0, force_tile=0):
         from split_kv_mla_gb300 import mla
         self.mla = mla
         self.kind, self.inp, self.device = kind, inp, device
-        self.force_splits = force_splits
+        self.force_splits, self.force_tile = force_splits, force_tile
         sms = mla.sm_count(device)
+        self.sms = sms
         if kind == "dense":
             self.plan = mla.mla_decode_plan(inp.batch, inp.q_len, inp.num_heads,
                                             inp.total_keys, sms)
@@ -275,8 +276,8 @@ class Runner:
                                  device=device)
             self.lse = torch.empty(inp.num_tokens, inp.num_heads, dtype=torch.float32,
                                    device=device)
-        if force_splits:
-            self.plan = mla.mla_plan_force_splits(self.plan, force_splits)
+        if force_splits or force_tile:
+            self.plan = self.plan_step()
         first = {k: v.to(device) for k, v in base.items()}
         self.copies = [first] + [{k: v.clone() for k, v in first.items()}
                                  for _ in range(copies - 1)]
@@ -291,6 +292,11 @@ class Runner:
         else:
             p = mla.mla_sparse_decode_plan(inp.num_tokens, inp.num_heads, inp.topk, self.sms,
                                            extra_topk=inp.extra_topk)
+        if self.force_tile:
+            # query rows per CTA (16, or 32 above 16 rows): tile sweeps
+            rows = p.q_len * p.num_heads
+            p.rows_per_cta = self.force_tile
+            p.head_blocks = p.grid_x = -(-rows // self.force_tile)
         return mla.mla_plan_force_splits(p, self.force_splits) if self.force_splits else p
 
     def call(self, d, pool, o, lse, stream, splits_only=False, plan=None):
@@ -332,8 +338,8 @@ class DcpRunner(Runner):
     shares (mla_dcp_lse_merge_ranks).  The other ranks' shares, which an
     all-gather would deliver, are computed once beforehand and stay in place."""
 
-    def __init__(self, shard, device, copies, force_splits=0):
-        super().__init__("dense", shard, device, copies, force_splits)
+    def __init__(self, shard, device, copies, force_splits=0, force_tile=0):
+        super().__init__("dense", shard, device, copies, force_splits, force_tile)
         self.kind = "dcp"
         base_inp, world = shard.dcp_base, shard.dcp_world
         self.world = world
@@ -678,8 +684,8 @@ def run_ours(args, rank, world, local_rank):
     # rotation copies: total input bytes > 4x L2
     dense = kind != "sparse"
     copies, per_copy = l2_copies(kind, inp, l2)
-    runner = (DcpRunner(inp, device, copies, args.splits) if kind == "dcp"
-              else Runner(kind, inp, device, copies, args.splits))
+    runner = (DcpRunner(inp, device, copies, args.splits, args.tile) if kind == "dcp"
+              else Runner(kind, inp, device, copies, args.splits, args.tile))
     stream = torch.cuda.Stream(device)
 
     # warm-up (eager) then graphs
@@ -753,6 +759,8 @@ def run_ours(args, rank, world, local_rank):
                          f"({copies * per_copy / 2**20:.0f} MiB > 4x L2 {l2 / 2**20:.0f} MiB)",
                    "timing": "CUDA-graph replays, CUDA events on the launch stream",
                    **({"forced_splits": args.splits} if args.splits else {}),
+                   **({"forced_rows_per_cta": args.tile} if args.tile else {}),
+                   "rows_per_cta": runner.plan.rows_per_cta,
                    "parallelism": f"replicas x{world}"},
         "us_per_call": ms_step * 1e3,
         "keys_per_s": keys_per_call(kind, inp) * world / (ms_step * 1e-3),
@@ -873,6 +881,8 @@ def main(argv=None):
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--splits", type=int, default=0,
                     help="force the split count instead of the planner's (split sweeps)")
+    ap.add_argument("--tile", type=int, default=0, choices=(0, 16, 32),
+                    help="force the query rows per CTA instead of the planner's (tile sweeps)")
     ap.add_argument("--workloads", default="all",
                     help="also time these workloads in the same run: all (single-GPU "
                          "runs), none, or a comma-separated list")

@@ -147,25 +147,28 @@ SplitChoice gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v
     return pick;
 }
 
-// Sparse split rule, following flashinfer.mla.cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits
+// Sparse split rule, after flashinfer.mla.cake_sparse_mla_sm120_dsv4_nvfp4_plan_splits
 // ("Measured split rules") with this kernel's geometry: a chunk is 64
 // candidates and a CTA should keep at least one 128-key block (two chunks).
-// While the unsplit grid covers at most 40 % of the SMs, take the largest
-// power-of-two split keeping the grid within the SM count and two chunks per
-// CTA (the page's cap is 80 % of the SMs; on GB300 a grid up to a full wave is
-// faster: 8 tokens x 64 heads take 16.7 us at 8 splits, 128 CTAs, against
-// 20.5 us at 4); on a full grid, split 16-chunk work in two when the doubled
-// grid ends in a wave at least half full; otherwise run unsplit.
+// The page splits only grids that cover at most 40 % of the SMs, and by powers
+// of two up to 80 % of them.  Re-derived on GB300: while the unsplit grid is
+// below one wave, take the largest split that keeps the grid within the SM
+// count and two chunks per CTA (64 heads, top-k 2048: 24 tokens 27.7 us at 3
+// splits against 31.4 at 2; 32 tokens 32.3 us at 2 against 42.8 unsplit; 12
+// tokens 20.0 at 6 against 21.2 at 4); on a full grid, split 16-chunk work in
+// two when the doubled grid ends in a wave at least half full; otherwise run
+// unsplit.
 int32_t sparse_splits(int64_t ctas, int64_t topk, int32_t sm_count)
 {
     const int64_t chunks = ceil_div(topk > 0 ? topk : 1, 64);
     if (chunks <= 2) return 1;
-    if (ctas * 10 <= (int64_t)sm_count * 4) {
-        int64_t ns = 1;
-        while (ctas * ns * 2 <= (int64_t)sm_count && chunks / (ns * 2) >= 2) ns *= 2;
+    if (ctas < sm_count) {
+        int64_t ns = (int64_t)sm_count / (ctas > 0 ? ctas : 1);
+        if (ns > chunks / 2) ns = chunks / 2;
+        if (ns < 1) ns = 1;
         return (int32_t)(ns < MLA_MAX_SPLITS ? ns : MLA_MAX_SPLITS);
     }
-    if (ctas >= sm_count && chunks == 16) {
+    if (chunks == 16) {
         const int64_t tail = (2 * ctas) % sm_count;
         if (tail == 0 || tail * 2 >= sm_count) return 2;
     }

@@ -7,7 +7,7 @@ unless --warm), and prints, per phase, when CTAs
 reach it relative to the launch's first CTA start (mean / min / max over CTAs,
 microseconds), plus the span of the CTAs' lives.
 
-    python -m split_kv_mla_gb300.trace c1q1 [c4-8 ...] [--splits N]
+    python -m split_kv_mla_gb300.trace c1q1 [c4-8 ...] [--splits N] [--tile 16|32]
 
 Workload names are bench.py's.  The traced build is for timelines only: its
 stamps cost a few global stores per CTA, and bench.py never loads it.
@@ -57,6 +57,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description="split-kernel phase timeline")
     ap.add_argument("workloads", nargs="*", default=["c1q1"])
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--tile", type=int, default=0, choices=(0, 16, 32),
+                    help="query rows per CTA (default: the planner's)")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--warm", action="store_true",
                     help="leave the inputs in L2 between launches (default: flush L2 first)")
@@ -72,6 +74,12 @@ def main(argv=None):
     for name in args.workloads:
         kind, inp, desc = bench.make_workload(name)
         runner = bench.Runner(kind, inp, device, 1, args.splits)
+        plan = runner.plan_step()
+        if args.tile:
+            rows = plan.q_len * plan.num_heads
+            plan.rows_per_cta = args.tile
+            plan.head_blocks = plan.grid_x = -(-rows // args.tile)
+        runner.plan = plan
         stream = torch.cuda.current_stream()
         spans = []
         flush = None if args.warm else torch.empty(512 << 20, dtype=torch.uint8, device=device)
@@ -79,7 +87,7 @@ def main(argv=None):
             lib.mla_trace_clear()
             if flush is not None:
                 flush.fill_(1)   # evict the inputs from L2 (512 MiB > 129 MB of L2)
-            runner.step(0, stream, splits_only=True)
+            runner.step(0, stream, splits_only=True, plan=plan)
             torch.cuda.synchronize()
             raw = np.zeros(WORDS, dtype=np.uint64)
             if lib.mla_trace_read(raw.ctypes.data, raw.size) != 0:

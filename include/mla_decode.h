@@ -251,7 +251,7 @@ int mla_decode_dcp_splits(const mla_plan_t* plan, const void* q_lat, const void*
  *   M = max_k lse_in[k, row];  w_k = 2^(lse_in[k, row] - M)
  *   out[row, :] = bf16(sum_k w_k parts_in[k, row, :] / sum_k w_k)
  *   lse_out[row] = M + log2 sum_k w_k           (when lse_out is non-NULL)
- * in the split-K reduce's fixed association (increasing k).  A row whose
+ * in a fixed association (each column sums its terms in increasing k).  A row whose
  * shares are all -inf gets out = 0 and lse_out = -inf.
  *   parts_in [cp_world, rows, d_v] (rank-major, as an all-gather leaves it),
  *            bf16 or fp32 as parts_dtype (MLA_DTYPE_BF16 / MLA_DTYPE_F32) says
@@ -333,9 +333,11 @@ int mla_workspace_partials(const mla_plan_t* plan, void* workspace, float** o_pa
  *   M = max_s lse_part[row, s];  w_s = 2^(lse_part[row, s] - M)
  *   o[row, :]  = bf16(out_scale * sum_s w_s o_part[row, s, :] / sum_s w_s)
  *   lse[row]   = M + log2 sum_s w_s            (when lse is non-NULL)
- * in a fixed association (each column sums its terms in increasing s; sum_s w_s
- * is 32 lane-strided partial sums joined by a butterfly), so the result does not
- * vary from call to call; a row whose partials are all -inf gets o = 0 and
+ * in a fixed association (sum_s w_s is 32 lane-strided partial sums joined by a
+ * butterfly; each column sums its terms in increasing s, or, above 16 splits
+ * and above 8 splits when rows <= 256, as four interleaved sums, s = g, g + 4,
+ * ... for g = 0..3, each in increasing s, added in increasing g), so the result
+ * does not vary from call to call; a row whose partials are all -inf gets o = 0 and
  * lse = -inf.  o_part fp32 [rows, num_splits, d_v] (normalized partials),
  * lse_part fp32 [rows, num_splits] base 2, o bf16 [rows, d_v]; d_v a multiple
  * of 8, num_splits in [1, MLA_MAX_SPLITS]; all 16-byte aligned.

@@ -10,8 +10,11 @@
 //   lse  = M + log2(sum_s w_s)      (-inf when every lse_s is -inf)
 // The fixed association: sum_s w_s is a per-lane sum over s = lane, lane + 32,
 // ... in increasing order followed by a butterfly over the 32 lanes (every lane
-// ends with the same bits, fp32 addition being commutative), and each output
-// column sums w_s o_s sequentially in increasing s.
+// ends with the same bits, fp32 addition being commutative).  Each output
+// column sums w_s o_s in G interleaved groups (group g: s = g, g + G, ... in
+// increasing order) and adds the group sums in increasing g; the reduce kernel
+// takes G = 4 above 16 splits, and above 8 splits for at most 256 rows, else
+// G = 1 (one sequential sum).
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -55,28 +58,28 @@ __device__ __forceinline__ void merge_weights(const float* lse, int ns, float* w
     wsum_out = part;
 }
 
-// acc + sum_s w[s] * op[s * stride + 0..3] for s = s0..ns-1 in increasing
-// order; loads of kUnroll splits are issued before their sums.
+// acc + sum_s w[s] * op[s * stride + 0..3] for s = s0, s0 + step, ... < ns in
+// increasing order; loads of kUnroll splits are issued before their sums.
 template <int kUnroll>
 __device__ __forceinline__ float4 merge_columns(const float* op, int64_t stride, int s0, int ns,
-                                                const float* w, float4 acc)
+                                                const float* w, float4 acc, int step = 1)
 {
     int s = s0;
-    for (; s + kUnroll <= ns; s += kUnroll) {
+    for (; s + (kUnroll - 1) * step < ns; s += kUnroll * step) {
         float4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-            v[u] = __ldcg(reinterpret_cast<const float4*>(op + (int64_t)(s + u) * stride));
+            v[u] = __ldcg(reinterpret_cast<const float4*>(op + (int64_t)(s + u * step) * stride));
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const float ws = w[s + u];
+            const float ws = w[s + u * step];
             acc.x += ws * v[u].x;
             acc.y += ws * v[u].y;
             acc.z += ws * v[u].z;
             acc.w += ws * v[u].w;
         }
     }
-    for (; s < ns; ++s) {
+    for (; s < ns; s += step) {
         const float ws = w[s];
         const float4 v = __ldcg(reinterpret_cast<const float4*>(op + (int64_t)s * stride));
         acc.x += ws * v.x;

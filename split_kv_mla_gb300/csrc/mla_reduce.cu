@@ -4,9 +4,14 @@
 // to 256 partitions).  The arithmetic and its fixed association are those of
 // mla_merge.cuh.  One CTA per row: each thread owns four consecutive columns and
 // reads them with 16-byte loads, so every split's row is one coalesced sweep.
-// The loads of the first kPrefetch splits' columns are in flight while warp 0
-// loads the row's LSEs and forms the weights, so a row with up to kPrefetch
-// splits costs one round trip to L2.
+// In the narrow form 128 threads each load every split's columns; in the wide
+// form (above 16 splits, or above 8 with at most 256 rows) four groups of 128
+// threads each take every fourth split (the interleaved groups of the fixed
+// association) and add their sums through shared memory.
+// A thread's first kPrefetch loads are in flight while warp 0 loads the row's
+// LSEs and forms the weights, so a row of up to 64 splits costs one round trip
+// to L2 (measured: B=1 H=64 S=131072 at 69 splits, the rest of the call after
+// the split kernel 8.8 us with one 128-thread group).
 //
 // The kernel is launched as a programmatic dependent of the split kernel: its
 // CTAs can be scheduled while the split kernel drains, and griddepcontrol.wait
@@ -23,8 +28,10 @@
 namespace mla {
 namespace {
 
-constexpr int kReduceThreads = 128;
-constexpr int kPrefetch = 16;
+constexpr int kReduceThreads = 128;   // threads of one split group (four columns each)
+constexpr int kPrefetch = 16;         // loads in flight per thread
+constexpr int kWideGroups = 4;        // split groups of a row in the wide form
+constexpr int kWideMaxRows = 256;     // ... also taken above 8 splits up to this many rows
 
 // Four merged columns scaled by f, stored as bf16 or fp32.
 __device__ __forceinline__ void store4(__nv_bfloat16* o, float4 acc, float f)
@@ -36,14 +43,15 @@ __device__ __forceinline__ void store4(float* o, float4 acc, float f)
     *reinterpret_cast<float4*>(o) = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
 }
 
-template <typename OutT>
-__global__ void __launch_bounds__(kReduceThreads)
+template <typename OutT, int G>
+__global__ void __launch_bounds__(kReduceThreads * G)
 splitk_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                      int64_t rows, int num_splits, int d_v, float out_scale,
                      OutT* __restrict__ o, float* __restrict__ lse)
 {
     __shared__ float w_s[MLA_MAX_SPLITS];
     __shared__ float fscale;
+    __shared__ float4 gsum[G > 1 ? G - 1 : 1][kReduceThreads];   // groups 1..G-1's sums
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // the next call's split kernel may be scheduled as soon as all rows started
@@ -51,14 +59,17 @@ splitk_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__
     const int64_t row = blockIdx.x;
     if (row >= rows) return;
     const int tid = threadIdx.x;
-    const int c = tid * 4;
+    const int g = tid / kReduceThreads;   // split group: s = g, g + G, ...
+    const int c = (tid % kReduceThreads) * 4;
     const bool cols = c < d_v;
     const float* op = o_part + row * (int64_t)num_splits * d_v + c;
     float4 v[kPrefetch];
 #pragma unroll
-    for (int u = 0; u < kPrefetch; ++u)
-        if (cols && u < num_splits)
-            v[u] = __ldcg(reinterpret_cast<const float4*>(op + (int64_t)u * d_v));
+    for (int u = 0; u < kPrefetch; ++u) {
+        const int sp = g + G * u;
+        if (cols && sp < num_splits)
+            v[u] = __ldcg(reinterpret_cast<const float4*>(op + (int64_t)sp * d_v));
+    }
     if (tid < 32) {
         float m, wsum;
         merge_weights(lse_part + row * num_splits, num_splits, w_s, m, wsum, tid);
@@ -68,21 +79,36 @@ splitk_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__
         }
     }
     __syncthreads();
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (cols) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < kPrefetch; ++u) {
-            if (u < num_splits) {
-                const float ws = w_s[u];
+            const int sp = g + G * u;
+            if (sp < num_splits) {
+                const float ws = w_s[sp];
                 acc.x += ws * v[u].x;
                 acc.y += ws * v[u].y;
                 acc.z += ws * v[u].z;
                 acc.w += ws * v[u].w;
             }
         }
-        if (num_splits > kPrefetch) acc = merge_columns<8>(op, d_v, kPrefetch, num_splits, w_s, acc);
-        store4(o + row * d_v + c, acc, fscale);
+        if (num_splits > G * kPrefetch)
+            acc = merge_columns<8>(op, d_v, g + G * kPrefetch, num_splits, w_s, acc, G);
     }
+    if constexpr (G > 1) {
+        if (g > 0) gsum[g - 1][tid % kReduceThreads] = acc;
+        __syncthreads();
+        if (g > 0) return;
+#pragma unroll
+        for (int k = 0; k < G - 1; ++k) {
+            const float4 x = gsum[k][tid];
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+        }
+    }
+    if (cols) store4(o + row * d_v + c, acc, fscale);
 }
 
 // Four columns of a share as fp32, from bf16 (8 bytes) or fp32 (16 bytes).
@@ -169,9 +195,14 @@ cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int
                                  bool out_f32, float* lse, cudaStream_t stream)
 {
     if (rows <= 0) return cudaSuccess;
+    // Four split groups when one group would need several round trips, and
+    // above 8 splits when the rows fit about one CTA per SM (measured on GB300:
+    // B=8 H=16 S=8192 at 16 splits, 128 rows, 18.4 -> 17.8 us per call; with
+    // 512 rows at 9 splits, B=8 H=64 S=131072, the wide form lost 285 -> 291).
+    const bool wide = num_splits > kPrefetch || (num_splits > 8 && rows <= kWideMaxRows);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rows, 1, 1);
-    cfg.blockDim = dim3(kReduceThreads, 1, 1);
+    cfg.blockDim = dim3(kReduceThreads * (wide ? kWideGroups : 1), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
@@ -179,11 +210,18 @@ cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (out_f32)
-        return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<float>, o_part, lse_part, rows,
-                                  num_splits, d_v, out_scale, static_cast<float*>(o), lse);
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<__nv_bfloat16>, o_part, lse_part, rows,
-                              num_splits, d_v, out_scale, static_cast<__nv_bfloat16*>(o), lse);
+    float* of = static_cast<float*>(o);
+    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+    if (wide)
+        return out_f32 ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<float, kWideGroups>, o_part,
+                                            lse_part, rows, num_splits, d_v, out_scale, of, lse)
+                       : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<__nv_bfloat16, kWideGroups>,
+                                            o_part, lse_part, rows, num_splits, d_v, out_scale, ob,
+                                            lse);
+    return out_f32 ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<float, 1>, o_part, lse_part,
+                                        rows, num_splits, d_v, out_scale, of, lse)
+                   : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<__nv_bfloat16, 1>, o_part,
+                                        lse_part, rows, num_splits, d_v, out_scale, ob, lse);
 }
 
 }  // namespace mla

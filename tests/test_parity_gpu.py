@@ -175,13 +175,22 @@ def test_split_count_does_not_change_the_answer_beyond_tolerance():
         compare(o, lse, ro, rl, f"forced ns={ns}")
 
 
-def test_splitk_reduce_matches_oracle_merge():
-    g = torch.Generator().manual_seed(4)
-    rows, ns, d_v = 37, 19, 512
+@pytest.mark.parametrize("rows,ns,d_v", [
+    (37, 19, 512),     # four split groups (above 16 splits)
+    (37, 7, 512),      # one group
+    (300, 12, 512),    # above 8 splits but more than 256 rows: one group
+    (200, 12, 448),    # above 8 splits, at most 256 rows: four groups
+    (5, 65, 512),      # four groups, past the first 64 splits' loads
+    (3, 256, 504),     # the largest split count; columns not a multiple of 512
+    (4, 9, 8),         # four groups over a narrow row
+])
+def test_splitk_reduce_matches_oracle_merge(rows, ns, d_v):
+    g = torch.Generator().manual_seed(4 + ns)
     parts = torch.randn(rows, ns, d_v, generator=g)
     lses = torch.randn(rows, ns, generator=g) * 6
-    lses[3, :] = -float("inf")
-    lses[5, 2:] = -float("inf")
+    lses[min(3, rows - 1), :] = -float("inf")        # a row with no key at all
+    if rows > 5:
+        lses[5, 2:] = -float("inf")
     o, l = mla.mla_splitk_reduce(parts.cuda(), lses.cuda(), out_scale=0.25)
     torch.cuda.synchronize()
     ro = np.zeros((rows, d_v))

@@ -335,7 +335,7 @@ int mla_workspace_partials(const mla_plan_t* plan, void* workspace, float** o_pa
  *   lse[row]   = M + log2 sum_s w_s            (when lse is non-NULL)
  * in a fixed association (sum_s w_s is 32 lane-strided partial sums joined by a
  * butterfly; each column sums its terms in increasing s, or, above 16 splits
- * and above 8 splits when rows <= 256, as four interleaved sums, s = g, g + 4,
+ * and above 8 splits when rows <= 128, as four interleaved sums, s = g, g + 4,
  * ... for g = 0..3, each in increasing s, added in increasing g), so the result
  * does not vary from call to call; a row whose partials are all -inf gets o = 0 and
  * lse = -inf.  o_part fp32 [rows, num_splits, d_v] (normalized partials),

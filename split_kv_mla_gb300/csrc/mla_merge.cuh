@@ -13,7 +13,7 @@
 // ends with the same bits, fp32 addition being commutative).  Each output
 // column sums w_s o_s in G interleaved groups (group g: s = g, g + G, ... in
 // increasing order) and adds the group sums in increasing g; the reduce kernel
-// takes G = 4 above 16 splits, and above 8 splits for at most 256 rows, else
+// takes G = 4 above 16 splits, and above 8 splits for at most 128 rows, else
 // G = 1 (one sequential sum).
 #pragma once
 #include <cstdint>

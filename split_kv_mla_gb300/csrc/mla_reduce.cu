@@ -5,7 +5,7 @@
 // mla_merge.cuh.  One CTA per row: each thread owns four consecutive columns and
 // reads them with 16-byte loads, so every split's row is one coalesced sweep.
 // In the narrow form 128 threads each load every split's columns; in the wide
-// form (above 16 splits, or above 8 with at most 256 rows) four groups of 128
+// form (above 16 splits, or above 8 with at most 128 rows) four groups of 128
 // threads each take every fourth split (the interleaved groups of the fixed
 // association) and add their sums through shared memory.
 // A thread's first kPrefetch loads are in flight while warp 0 loads the row's
@@ -31,7 +31,7 @@ namespace {
 constexpr int kReduceThreads = 128;   // threads of one split group (four columns each)
 constexpr int kPrefetch = 16;         // loads in flight per thread
 constexpr int kWideGroups = 4;        // split groups of a row in the wide form
-constexpr int kWideMaxRows = 256;     // ... also taken above 8 splits up to this many rows
+constexpr int kWideMaxRows = 128;     // ... also taken above 8 splits up to this many rows
 
 // Four merged columns scaled by f, stored as bf16 or fp32.
 __device__ __forceinline__ void store4(__nv_bfloat16* o, float4 acc, float f)
@@ -196,9 +196,10 @@ cudaError_t launch_splitk_reduce(const float* o_part, const float* lse_part, int
 {
     if (rows <= 0) return cudaSuccess;
     // Four split groups when one group would need several round trips, and
-    // above 8 splits when the rows fit about one CTA per SM (measured on GB300:
-    // B=8 H=16 S=8192 at 16 splits, 128 rows, 18.4 -> 17.8 us per call; with
-    // 512 rows at 9 splits, B=8 H=64 S=131072, the wide form lost 285 -> 291).
+    // above 8 splits for at most 128 rows (measured on GB300: B=8 H=16 S=8192
+    // at 16 splits, 128 rows, 18.4 -> 17.8 us per call; the wide form lost
+    // with 256 rows at 9 splits, sparse T=4 H=64, 11.9 -> 13.5, and with 512
+    // rows at 9 splits, B=8 H=64 S=131072, 285 -> 291).
     const bool wide = num_splits > kPrefetch || (num_splits > 8 && rows <= kWideMaxRows);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rows, 1, 1);

@@ -178,8 +178,8 @@ def test_split_count_does_not_change_the_answer_beyond_tolerance():
 @pytest.mark.parametrize("rows,ns,d_v", [
     (37, 19, 512),     # four split groups (above 16 splits)
     (37, 7, 512),      # one group
-    (300, 12, 512),    # above 8 splits but more than 256 rows: one group
-    (200, 12, 448),    # above 8 splits, at most 256 rows: four groups
+    (300, 12, 512),    # above 8 splits but more than 128 rows: one group
+    (120, 12, 448),    # above 8 splits, at most 128 rows: four groups
     (5, 65, 512),      # four groups, past the first 64 splits' loads
     (3, 256, 504),     # the largest split count; columns not a multiple of 512
     (4, 9, 8),         # four groups over a narrow row

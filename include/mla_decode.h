@@ -172,9 +172,8 @@ int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
  * scale multiplies the raw q.k dot product of dequantized rows (typically
  * (512+64)^-0.5); kv_scale dequantizes the pool.  Rows are copied in 128-key
  * blocks: the keys of a block that a call masks (past a request's length, or
- * invalid sparse entries) are copied from pool row 0 and weighted by zero, so
- * row 0 must hold finite e4m3fn bytes (no NaN code 0x7f / 0xff), like every
- * row the page table names.
+ * invalid sparse entries) become zero rows without reading the pool, so only
+ * the rows the page table names need finite e4m3fn bytes.
  */
 int mla_decode(const mla_plan_t* plan, const void* q_lat, const void* q_pe,
                const void* pool, int64_t pool_rows, const int32_t* seq_lens,

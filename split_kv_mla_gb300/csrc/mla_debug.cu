@@ -37,7 +37,8 @@ gather_probe_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
     __syncthreads();
     // Every row of the stage is gathered (rows past n and out-of-range slots
-    // read pool row 0), so the byte count is the whole stage.
+    // at row coordinate -1, outside the tensor: the copy fills them with
+    // zeros), so the byte count is the whole stage.
     if (tid == 0) mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes);
     for (int item = lane; item < 8 * kBoxes; item += 32) {
         const int g = warp * 8 + item / kBoxes;   // four-row group
@@ -46,8 +47,8 @@ gather_probe_kernel(const __grid_constant__ CUtensorMap tm_lat,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int64_t row = base + 4 * g + i;
-            const int32_t v = row < n ? __ldg(idx + row) : 0;
-            r[i] = (v >= 0 && (int64_t)v < pool_rows) ? v : 0;
+            const int32_t v = row < n ? __ldg(idx + row) : -1;
+            r[i] = (v >= 0 && (int64_t)v < pool_rows) ? v : -1;
         }
         if (c < 4)
             tma_gather4(smem + c * kProbeRows * 128 + g * 512, &tm_lat, c * 128, r[0], r[1], r[2],
@@ -70,9 +71,8 @@ gather_probe_kernel(const __grid_constant__ CUtensorMap tm_lat,
     for (int e = tid; e < nr * kChunks; e += kProbeWarps * 32) {
         const int r = e / kChunks, c16 = e % kChunks;
         const int64_t row = base + r;
-        const int32_t v = __ldg(idx + row);
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (ok && v >= 0 && (int64_t)v < pool_rows)
+        if (ok)   // out-of-range slots: the rows the copy filled
             val = *reinterpret_cast<const uint4*>(smem + tile_offset(r, c16 * 16, kProbeRows));
         *reinterpret_cast<uint4*>(out + row * kRowBytes + c16 * 16) = val;
     }

@@ -788,11 +788,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     auto slot_ok = [&](int32_t v, bool ex) {
         return v >= 0 && (int64_t)v < (ex ? a.extra_rows : a.pool_rows);
     };
-    // Slots to gather: masked or invalid keys read row 0 of their cache
-    // (finite bytes, p = 0).
+    // Slots to gather: masked or invalid keys take row coordinate -1, outside
+    // the tensor, where the copy fills the row with zeros (p = 0 for them, and
+    // no pool row is read).
     auto fix_slots = [&](Slots r) -> Slots {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) r.v[i] = slot_ok(r.v[i], r.ex) ? r.v[i] : 0;
+        for (int i = 0; i < 4; ++i) r.v[i] = slot_ok(r.v[i], r.ex) ? r.v[i] : -1;
         return r;
     };
     // Validity of row tid (a dense slot out of range is reported, not read).
@@ -809,8 +810,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     // end are not fetched from block 2 on: their rows are masked, and the stage
     // still holds block j-2's rows there (finite bytes; the copy engine's issue
     // rate, not DRAM, bounds a block, so a short last block costs less).  The
-    // stages' first fills copy every group (row 0 for masked rows), so no row of
-    // a stage is ever read uninitialised.
+    // stages' first fills copy every group (zero rows for masked keys), so no
+    // row of a stage is ever read uninitialised.
     auto issue = [&](int j, const Slots& sl, int rowok) {
         const int st = j & 1;
         const int nk = min(kBlockN, k1 - (k0 + j * kBlockN));

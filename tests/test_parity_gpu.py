@@ -175,6 +175,31 @@ def test_split_count_does_not_change_the_answer_beyond_tolerance():
         compare(o, lse, ro, rl, f"forced ns={ns}")
 
 
+def test_masked_keys_read_no_pool_row():
+    # NaN bytes (e4m3fn 0x7f) in every pool row that no key names, row 0
+    # included: masked keys (past each request's length in a split's last
+    # block) must not bring them in
+    import dataclasses
+    inp = gen.dense_inputs(3, 1, 16, [1000, 77, 600], seed=61, extra_slots=50)
+    idx = inp.kv_indices.clone()
+    used = torch.zeros(inp.pool.shape[0], dtype=torch.bool)
+    used[idx.long()] = True
+    spare = int(torch.nonzero(~used)[0])
+    idx[idx == 0] = spare                      # row 0 named by no key
+    used = torch.zeros_like(used)
+    used[idx.long()] = True
+    assert not used[0] and int((~used).sum()) == 50
+    pool = inp.pool.clone()
+    pool[~used] = 0x7F
+    inp2 = dataclasses.replace(inp, pool=pool, kv_indices=idx)
+    plan = mla.mla_plan_force_splits(
+        mla.mla_decode_plan(3, 1, 16, inp.total_keys, mla.sm_count()), 3)
+    o, lse, _ = run_dense(inp2, plan=plan)
+    assert torch.isfinite(o.float()).all()
+    ro, rl = oracle.dense_decode(inp2)
+    compare(o, lse, ro, rl, "NaN bytes in unnamed rows")
+
+
 @pytest.mark.parametrize("rows,ns,d_v", [
     (37, 19, 512),     # four split groups (above 16 splits)
     (37, 7, 512),      # one group

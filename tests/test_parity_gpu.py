@@ -200,6 +200,28 @@ def test_masked_keys_read_no_pool_row():
     compare(o, lse, ro, rl, "NaN bytes in unnamed rows")
 
 
+def test_invalid_sparse_entries_read_no_pool_row():
+    # NaN bytes in every pool row no valid entry names, row 0 included; the
+    # invalid (-1) entries and a short top-k must not bring them in
+    import dataclasses
+    inp = gen.sparse_inputs(4, 64, 300, pool_rows=2000, seed=62, invalid_frac=0.3)
+    idx = inp.indices.clone()
+    used = torch.zeros(inp.pool.shape[0], dtype=torch.bool)
+    used[idx[idx >= 0].long()] = True
+    spare = int(torch.nonzero(~used)[0])
+    idx[idx == 0] = spare
+    used = torch.zeros_like(used)
+    used[idx[idx >= 0].long()] = True
+    assert not used[0] and int((idx < 0).sum()) > 0
+    pool = inp.pool.clone()
+    pool[~used] = 0x7F
+    inp2 = dataclasses.replace(inp, pool=pool, indices=idx)
+    o, lse, _ = run_sparse(inp2)
+    assert torch.isfinite(o.float()).all()
+    ro, rl = oracle.sparse_decode(inp2)
+    compare(o, lse, ro, rl, "NaN bytes in unnamed rows, sparse")
+
+
 @pytest.mark.parametrize("rows,ns,d_v", [
     (37, 19, 512),     # four split groups (above 16 splits)
     (37, 7, 512),      # one group

@@ -36,7 +36,7 @@ inline bool rows_per_cta_ok(int64_t rows, int32_t rpc)
 // constants come from phase traces and split sweeps of this kernel on GB300.
 constexpr double kBlockUs16 = 2.1;     // a 128-key block, 16 query rows per CTA (latency-bound)
 constexpr double kBlockUs32 = 2.2;     // ... 32 query rows per CTA
-constexpr double kGather32 = 4.4e6;    // bytes/us gathered GPU-wide by 32-row CTAs (a
+constexpr double kGather32 = 5.0e6;    // bytes/us gathered GPU-wide by 32-row CTAs (a
                                        // request's head blocks gather the same rows); 16-row
                                        // CTAs measured no GPU-wide cap up to a full wave
 constexpr double kCtaUs = 6.0;         // start-up to the first QK, and the epilogue
@@ -122,6 +122,7 @@ SplitChoice gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v
     const double block_us = rows_per_cta == 16 ? kBlockUs16 : kBlockUs32;
     const double us_per_cta_block =
         rows_per_cta == 16 ? 0.0 : (double)kBlockN * row_bytes / kGather32;
+    const double cta_us = kCtaUs + (rows_per_cta == 16 ? 0.0 : kFirstBlockUs32);
     double best = 0.0;
     SplitChoice pick{1, 1, 0.0};
     auto consider = [&](int64_t ns, int32_t mc) {
@@ -130,7 +131,7 @@ SplitChoice gb300_splits(int64_t tiles, int64_t keys, int64_t items, int32_t d_v
         const double bpc = (double)ceil_div(blocks, ns);
         auto wave_us = [&](int64_t active) {
             const double b = (double)active * us_per_cta_block;
-            return bpc * (b > block_us ? b : block_us) + kCtaUs;
+            return bpc * (b > block_us ? b : block_us) + cta_us;
         };
         double t = (double)(ctas / wave) * wave_us(wave);
         if (ctas % wave != 0) t += wave_us(ctas % wave);
@@ -338,12 +339,13 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
     };
     // Above 16 rows, the 32-row tile against the 16-row one (twice the head
     // blocks, each gathering the same rows): the smaller tile wins where a
-    // CTA's work is short, since a 32-row CTA starts about 5 us later.
+    // CTA's work is short, since a 32-row CTA starts about 5 us later (a cost
+    // the model charges each wave of 32-row CTAs).
     int32_t rpc = rows_per_cta_for(rows);
     SplitChoice ch = choose(rpc);
     if (rpc == 32) {
         const SplitChoice ch16 = choose(16);
-        if (ch16.us < ch.us + kFirstBlockUs32) {
+        if (ch16.us < ch.us) {
             rpc = 16;
             ch = ch16;
         }

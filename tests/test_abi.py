@@ -262,7 +262,9 @@ def test_long_first_only_when_the_grid_outlasts_a_wave():
     (8, 1, 16, 8192, 16),       # c1 q_len=1
     (8, 4, 16, 8192, 8),        # c1 q_len=4
     (8, 1, 64, 131072, 9),      # c2 8x131072 (one wave)
-    (1, 1, 64, 131072, 69),     # c2 1x131072 (64 and 74 measured within 1 %)
+    (1, 1, 64, 131072, 74),     # c2 1x131072 (48.99 us; 69 splits 50.76)
+    (1, 1, 64, 65536, 74),      # 32.71 us; 64 splits 34.01
+    (4, 1, 64, 16384, 19),      # 33.06 us; 16 splits 34.46
     (2, 1, 64, 65536, 37),      # c2 2x65536
     (16, 1, 64, 131072, 9),     # c2 16x131072
     (64, 1, 128, 16896, 1),     # c3's shape (mean length)

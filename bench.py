@@ -446,10 +446,11 @@ def e2e_measure(runner, stream, steps):
     (one copy of a packed buffer), runs the decode, and copies o and lse back
     (one copy of a packed buffer); the KV pool is resident cache state and
     rotates over the device copies like the main arm.  As a serving loop would,
-    the steps are replayed from a CUDA graph and pipelined over two sets of
-    buffers: step i's input copy (one copy stream) and step i-1's result copy
-    (another) overlap the decode of the step in between, and a buffer is reused
-    only after the step two back has finished with it."""
+    the steps are replayed from a CUDA graph (60 or more steps per replay) and
+    pipelined over two sets of buffers: step i's input copy (one copy stream)
+    and step i-1's result copy (another) overlap the decode of the step in
+    between, and a buffer is reused only after the step two back has finished
+    with it."""
     inp = runner.inp
     names = runner.input_names()
     src = [getattr(inp, n).contiguous() for n in names]
@@ -505,7 +506,9 @@ def e2e_measure(runner, stream, steps):
         stream.wait_stream(c_in)
         stream.wait_stream(c_out)
 
-    n = max(2, len(copies))
+    # one graph holds whole rotations of the input copies, at least 60 steps,
+    # so that the pipeline's fill and drain at each replay cost little
+    n = max(2, len(copies)) * max(1, -(-60 // max(2, len(copies))))
     with torch.cuda.stream(stream):
         run(3)
     torch.cuda.synchronize()

@@ -31,6 +31,14 @@ def test_build_is_up_to_date():
     assert os.path.exists(mla_build.build())
 
 
+@needs_nvcc
+def test_gather_rate_probe_builds():
+    # the measurement program behind profiles/gather_rate_576B_rows.md compiles
+    # for sm_103a (it runs on a GPU only)
+    from split_kv_mla_gb300 import gather_rate
+    assert os.path.exists(gather_rate.build())
+
+
 def test_every_declared_symbol_is_exported(lib):
     names = mla.declared_symbols()
     assert {"mla_decode_plan", "mla_decode", "mla_sparse_decode", "mla_splitk_reduce",

@@ -244,8 +244,9 @@ void carve(const mla_plan_t* plan, void* ws, int64_t items, SplitArgs* a)
     }
 }
 
-// A plan's launch geometry must be the one the planner derives from its shape
-// and split count: the kernels index the workspace and the outputs by it.
+// A plan's launch geometry must follow from its shape, its tile (16 rows per
+// CTA, or 32 above 16 rows) and its split count: the kernels index the
+// workspace and the outputs by it.
 bool variant_ok(const mla_plan_t* plan)
 {
     if (plan->variant != kVariantTc) return false;

@@ -91,3 +91,26 @@ def test_call_with_no_key_at_all(batch, q_len, heads, ns):
     o, lse, _ = run_dense(inp, plan=plan, ws=ws)
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
     assert mla.mla_read_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_second_cache_calls(seed):
+    rng = np.random.default_rng(5000 + seed)
+    tokens = int(rng.integers(1, 5))
+    heads = int(rng.choice([16, 32, 64, 128]))
+    topk = int(rng.integers(0, 700))
+    extra = int(rng.integers(1 if topk == 0 else 0, 300))
+    rows = int(rng.integers(max(topk, 1), 5000))
+    xrows = int(rng.integers(max(extra, 1), 3000))
+    inp = gen.sparse_extra_inputs(tokens, heads, topk, extra, rows, xrows, seed=6000 + seed,
+                                  invalid_frac=float(rng.choice([0.0, 0.2])))
+    plan = mla.mla_sparse_decode_plan(tokens, heads, topk, mla.sm_count(), extra_topk=extra)
+    plan = _shape_plan(plan, rng, topk + extra)
+    o, lse = mla.mla_sparse_decode_extra(plan, inp.q_nope.cuda(), inp.q_pe.cuda(),
+                                         inp.pool.cuda(), inp.indices.cuda(),
+                                         inp.extra_pool.cuda(), inp.extra_indices.cuda(),
+                                         inp.scale, inp.kv_scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.sparse_extra_decode(inp)
+    compare(o, lse, ro, rl, f"second cache seed {seed}: T={tokens} H={heads} topk={topk} "
+                            f"extra={extra} ns={plan.num_splits} rpc={plan.rows_per_cta}")

@@ -139,6 +139,12 @@ def kv_bytes_per_call(kind, inp) -> int:
     return keys_per_call(kind, inp) * row_bytes(kind)
 
 
+def workload_label(name, kind, desc) -> str:
+    """The config's workload string, the same in both arms."""
+    return (f"{name}: dense MLA decode {desc}" if kind != "sparse"
+            else f"{name}: sparse top-k MLA decode {desc}")
+
+
 def row_bytes(kind) -> int:
     return ROW_BYTES["sparse" if kind == "sparse" else "dense"]
 
@@ -685,7 +691,6 @@ def run_ours(args, rank, world, local_rank):
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     # rotation copies: total input bytes > 4x L2
-    dense = kind != "sparse"
     copies, per_copy = l2_copies(kind, inp, l2)
     runner = (DcpRunner(inp, device, copies, args.splits, args.tile) if kind == "dcp"
               else Runner(kind, inp, device, copies, args.splits, args.tile))
@@ -754,8 +759,7 @@ def run_ours(args, rank, world, local_rank):
                         if pages_baseline_gbs(args.workload) else None),
         "dtype": "e4m3fn-kv/bf16-q(e4m3 hi+mid[+lo])/p(e4m3 hi+lo)/fp32-acc",
         "data": "synthetic (seeded; N(0,1) bf16 queries, N(0,1)/kv_scale e4m3fn pool, shuffled page_size-1 slots)",
-        "config": {"workload": f"{args.workload}: dense MLA decode {desc}" if dense
-                   else f"{args.workload}: sparse top-k MLA decode {desc}",
+        "config": {"workload": workload_label(args.workload, kind, desc),
                    "kv_bytes_per_call": bytes_call, "keys_per_call": keys_per_call(kind, inp),
                    "num_splits": runner.plan.num_splits, "head_blocks": runner.plan.head_blocks,
                    "l2": f"inputs rotated over {copies} device copies "
@@ -837,7 +841,9 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, same recipe as the GPU arm)",
-        "config": {"workload": f"{args.workload}: {desc}", "sample": sample},
+        "config": {"workload": workload_label(args.workload, kind, desc),
+                   "kv_bytes_per_call": kv_bytes_per_call(kind, inp),
+                   "keys_per_call": keys_per_call(kind, inp), "sample": sample},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.cpu_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

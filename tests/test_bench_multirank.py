@@ -141,6 +141,13 @@ def test_bench_gpus_2_spawns_ranks_and_prints_one_line():
     assert len(lines) == 1
     out = json.loads(lines[0])
     assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
+    # the same workload label and sizes as the GPU arm's config
+    sys.path.insert(0, ROOT)
+    import bench
+    kind, inp, desc = bench.make_workload("c0")
+    assert out["config"]["workload"] == bench.workload_label("c0", kind, desc)
+    assert out["config"]["kv_bytes_per_call"] == bench.kv_bytes_per_call(kind, inp)
+    assert out["config"]["keys_per_call"] == bench.keys_per_call(kind, inp)
 
 
 def test_every_sweep_workload_name_parses():

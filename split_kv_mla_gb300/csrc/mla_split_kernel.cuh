@@ -34,13 +34,13 @@
 //   seven warps; warp 7 issues the tcgen05.mma (kind::f8f6f4, fp32 accumulators
 //   in TMEM) and commits to mbarriers; warps 8-11 and 12-15 are two softmax sets,
 //   each owning half the query rows, and warp w % 4 of a set owns TMEM lanes
-//   32 (w % 4)..+31 (one key per thread).  Measured on GB300, a warp issues one
-//   gather4 about every 100 cycles, so a block's issue time falls with the number
-//   of issuing warps (per SM, random 576-byte rows gather at ~38 GB/s from four
-//   warps, ~54 GB/s from eight); and one softmax warp per SM sub-partition left
-//   its dependent chains exposed, so every key has two.  Registers move with
-//   setmaxnreg from warpgroups 0-1 (64 per thread) to the softmax warpgroups
-//   (192).
+//   32 (w % 4)..+31 (one key per thread).  Measured on GB300, a block's 160
+//   gather4 copies take ~3,800 SM cycles to issue from seven warps (~3,200 from
+//   sixteen), and an SM streams random 576-byte rows at ~30-35 GB/s: the copy
+//   engine, not the number of issuing warps, sets the rate.  One softmax warp per
+//   SM sub-partition left its dependent chains exposed, so every key has two.
+//   Registers move with setmaxnreg from warpgroups 0-1 (64 per thread) to the
+//   softmax warpgroups (192).
 // * Lazy rescaling.  Each row keeps a reference m that bounds its logits; p is
 //   2^(s - m).  A block only moves the reference of a row whose logits exceed it
 //   by more than kTau (then to the block maximum plus kHeadroom, so the next

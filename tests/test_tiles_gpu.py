@@ -84,3 +84,17 @@ def test_planner_tile_on_small_h64_decode_matches_oracle():
     assert plan.rows_per_cta == 16 and plan.head_blocks == 4
     ro, rl = oracle.dense_decode(inp)
     compare(o, lse, ro, rl, "planner tile")
+
+
+@pytest.mark.parametrize("rpc", [16, 32])
+def test_many_head_blocks_per_request(rpc):
+    # 8 draft rows x 128 heads = 1024 rows per request: 64 or 32 head blocks,
+    # ragged windows, a short request and a forced split count
+    inp = gen.dense_inputs(2, 8, 128, [900, 5], seed=77 + rpc)
+    base = mla.mla_plan_force_splits(
+        mla.mla_decode_plan(2, 8, 128, inp.total_keys, mla.sm_count()), 3)
+    plan = _with_tile(base, rpc)
+    assert plan.head_blocks == 1024 // rpc
+    o, lse, _ = run_dense(inp, plan=plan)
+    ro, rl = oracle.dense_decode(inp)
+    compare(o, lse, ro, rl, f"1024 rows per request, rows_per_cta={rpc}")

@@ -58,7 +58,8 @@ extern "C" {
 #define MLA_OK 0
 #define MLA_ERR_INVALID_ARG (-1)         /* null pointer, negative size, plan/shape mismatch */
 #define MLA_ERR_UNSUPPORTED_SHAPE (-2)   /* d_v/d_rope not (512,64) dense or (448,64) sparse,
-                                            heads outside [1,128], too many splits */
+                                            heads outside [1,128], too many splits,
+                                            more than 65535 requests or tokens */
 #define MLA_ERR_MISALIGNED (-3)          /* a buffer is not 16-byte aligned */
 #define MLA_ERR_WORKSPACE_TOO_SMALL (-4) /* workspace_bytes < plan->workspace_bytes */
 #define MLA_ERR_UNSUPPORTED_DEVICE (-5)  /* current device is not compute capability 10.3 */
@@ -132,7 +133,9 @@ typedef struct {
  * value); sm_count = the device's multiProcessorCount.  d_v must be 512 and
  * d_rope 64 (README, "Constraints / MLA decode": kv_lora_rank 512,
  * qk_rope_head_dim 64); num_heads in [1, 128] (same passage: H 1..128); any
- * q_len >= 1.  Writes *out and returns MLA_OK, or a status.
+ * q_len >= 1 with q_len * num_heads <= 2^20; batch <= 65535 (the requests are
+ * the split grid's third dimension).  Writes *out and returns MLA_OK, or a
+ * status.
  */
 int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t total_keys,
                     int32_t d_v, int32_t d_rope, int32_t sm_count, mla_plan_t* out);
@@ -146,7 +149,7 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
  * cache, 0 without one (mla_sparse_decode_extra).  max_splits caps num_splits
  * (0 = MLA_MAX_SPLITS).  Every split count from 1 up is valid for this kernel
  * (a split may even be empty), so a small cap costs speed only and is never an
- * error.
+ * error.  num_tokens <= 65535 (the tokens are the split grid's third dimension).
  */
 int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
                            int32_t extra_topk, int32_t d_v, int32_t d_rope, int32_t sm_count,

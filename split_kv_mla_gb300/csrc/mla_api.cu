@@ -12,6 +12,7 @@ namespace {
 constexpr int kDenseDv = 512, kDenseDr = 64;
 constexpr int kSparseDv = 448, kSparseDr = 64;
 constexpr int kMaxHeads = 128;
+constexpr int32_t kMaxBatch = 65535;   // requests (tokens) are the split grid's z dimension
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Split-kernel geometry: 128 keys per block; 16 query rows per CTA when a
@@ -251,6 +252,7 @@ bool variant_ok(const mla_plan_t* plan)
 {
     if (plan->variant != kVariantTc) return false;
     if (plan->q_len < 1 || plan->num_heads < 1 || plan->batch < 0) return false;
+    if (plan->batch > kMaxBatch) return false;
     const int64_t rows = (int64_t)plan->q_len * plan->num_heads;
     if (rows > (1 << 20)) return false;
     if (!rows_per_cta_ok(rows, plan->rows_per_cta) || plan->block_n != kBlockN ||
@@ -329,7 +331,8 @@ int mla_decode_plan(int32_t batch, int32_t q_len, int32_t num_heads, int64_t tot
 {
     if (!out || batch < 0 || q_len < 1 || total_keys < 0 || sm_count < 1)
         return MLA_ERR_INVALID_ARG;
-    if (d_v != kDenseDv || d_rope != kDenseDr || num_heads < 1 || num_heads > kMaxHeads)
+    if (d_v != kDenseDv || d_rope != kDenseDr || num_heads < 1 || num_heads > kMaxHeads ||
+        batch > kMaxBatch)
         return MLA_ERR_UNSUPPORTED_SHAPE;
     const int64_t rows = (int64_t)q_len * num_heads;
     if (rows > (1 << 20)) return MLA_ERR_UNSUPPORTED_SHAPE;
@@ -368,7 +371,8 @@ int mla_sparse_decode_plan(int32_t num_tokens, int32_t num_heads, int32_t topk,
     if (!out || num_tokens < 0 || topk < 0 || extra_topk < 0 || sm_count < 1 || max_splits < 0)
         return MLA_ERR_INVALID_ARG;
     if ((int64_t)topk + extra_topk + 3 > (1LL << 30)) return MLA_ERR_UNSUPPORTED_SHAPE;
-    if (d_v != kSparseDv || d_rope != kSparseDr || num_heads < 1 || num_heads > kMaxHeads)
+    if (d_v != kSparseDv || d_rope != kSparseDr || num_heads < 1 || num_heads > kMaxHeads ||
+        num_tokens > kMaxBatch)
         return MLA_ERR_UNSUPPORTED_SHAPE;
     const int32_t cap = max_splits == 0 ? MLA_MAX_SPLITS
                                         : (max_splits < MLA_MAX_SPLITS ? max_splits : MLA_MAX_SPLITS);

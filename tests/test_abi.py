@@ -130,6 +130,22 @@ def test_plan_rejections(lib):
         mla.mla_sparse_decode_plan(4, 64, 2048, 152, d_v=512)
 
 
+def test_plans_cap_requests_and_tokens_at_the_grid_limit(lib):
+    # requests (tokens) are the split grid's z dimension, at most 65535
+    assert mla.mla_decode_plan(65535, 1, 16, 65535 * 64, 152).grid_z == 65535
+    assert mla.mla_sparse_decode_plan(65535, 64, 2048, 152).grid_z == 65535
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_plan(65536, 1, 16, 65536 * 64, 152)
+    assert e.value.status == -2
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_sparse_decode_plan(65536, 64, 2048, 152)
+    assert e.value.status == -2
+    # a plan edited past the limit is refused before any launch
+    q = mla.mla_plan_t.from_buffer_copy(mla.mla_decode_plan(4, 1, 16, 256, 152))
+    q.batch = q.grid_z = 70000
+    assert _call_decode(lib, q, ws_bytes=1 << 30, batch=70000) == -1
+
+
 def test_sparse_plan_max_splits(lib):
     p = mla.mla_sparse_decode_plan(1, 64, 2048, 152)
     assert p.num_splits >= 1 and p.total_keys == 2048

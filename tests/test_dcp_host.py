@@ -96,16 +96,19 @@ def _worker(rank, world, port, out):
         dist.destroy_process_group()
 
 
-def test_exchange_and_merge_world_size_2_gloo():
+@pytest.mark.parametrize("world", [2, 4])
+def test_exchange_and_merge_gloo(world):
+    # world 4: the 2-key request has no positions on ranks 2 and 3, whose
+    # shares are then empty (o = 0, lse = -inf) and must merge away
     ctx = mp.get_context("spawn")
     with ctx.Manager() as mgr:
         out = mgr.dict()
-        mp.start_processes(_worker, args=(2, _free_port(), out), nprocs=2, join=True,
+        mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, join=True,
                            start_method="spawn")
         res = dict(out)
-    assert sorted(res) == [0, 1]
+    assert sorted(res) == list(range(world))
     for shape, o_err, l_err, fin_ok in res.values():
-        assert shape == (2, 9, 2, 32)
+        assert shape == (world, 9, 2, 32)
         assert o_err <= 1e-12 and l_err <= 1e-12 and fin_ok
 
 

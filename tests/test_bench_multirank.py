@@ -1,7 +1,7 @@
 """Host logic of bench.py's multi-rank path (independent replicas under
-torch.distributed), run with world size 2 over gloo on the CPU: every rank gets
-the slowest rank's time, the whole-job value counts every rank's work over that
-time, and the reference arm prints from rank 0 only."""
+torch.distributed), run with world sizes 2 and 4 over gloo on the CPU: every
+rank gets the slowest rank's time, the whole-job value counts every rank's work
+over that time, and the reference arm prints from rank 0 only."""
 import os
 import socket
 import sys
@@ -33,13 +33,15 @@ def _worker(rank, world, port, out):
         dist.destroy_process_group()
 
 
-def test_max_over_ranks_world_size_2_gloo():
+@pytest.mark.parametrize("world", [2, 4])
+def test_max_over_ranks_gloo(world):
     ctx = mp.get_context("spawn")
     with ctx.Manager() as mgr:
         out = mgr.dict()
-        mp.start_processes(_worker, args=(2, _free_port(), out), nprocs=2, join=True,
+        mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, join=True,
                            start_method="spawn")
-        assert dict(out) == {0: 3.5, 1: 3.5}
+        slowest = 1.5 + 2.0 * (world - 1)
+        assert dict(out) == {r: slowest for r in range(world)}
 
 
 def test_single_rank_needs_no_process_group():

@@ -103,7 +103,7 @@ constexpr int kTraceCtas = 8192;
 // ... followed by per-block events of the first kTraceBlockCtas CTAs.
 constexpr int kTraceBlockCtas = 4;
 constexpr int kTraceBlocks = 64;
-constexpr int kTraceBlockEvents = 6;
+constexpr int kTraceBlockEvents = 8;
 constexpr int kTraceWords =
     kTraceCtas * kTraceSlots + kTraceBlockCtas * kTraceBlocks * kTraceBlockEvents;
 

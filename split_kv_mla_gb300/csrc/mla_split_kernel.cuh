@@ -103,8 +103,8 @@ __device__ __forceinline__ void trace_block(const SplitArgs& a, int j, int e)
 #define MLA_BLOCK_STAMP(j, e) ((void)0)
 #endif
 // Block events: 0 gather warp 0 starts issuing the block, 1 it has issued its
-// copies, 2 QK issued, 3 S loaded by the first softmax warp, 4 its P
-// published, 5 P.V issued.
+// copies, 2 QK issued, 3 S loaded by the first softmax set's first warp, 4 its
+// P published, 5 P.V issued, 6 and 7 as 3 and 4 for the second softmax set.
 // Stamp slots: 0 CTA start, 1 after the wait for the preceding kernel,
 // 2 first gather issued, 3 first QK issued, 4 last P.V issued, 5 epilogue has
 // O, 6 rows staged, 7 rows stored, 8 end, 9 query tile written (first query
@@ -1214,7 +1214,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                 const uint32_t sa = tmem + lane_addr + C::kColS + st * NQ + r0;
                 if (q3) load_rows<R>(sa, sa + N, sa + 2 * N, s);
                 else load_rows<R>(sa, sa + N, s);
-                if (warp == kSoftmaxWarp0 && lane == 0) MLA_BLOCK_STAMP(blk, 3);
+                if ((warp & 3) == 0 && lane == 0) MLA_BLOCK_STAMP(blk, warp == kSoftmaxWarp0 ? 3 : 6);
             } else {
 #pragma unroll
                 for (int n = 0; n < R; ++n) s[n] = -CUDART_INF_F;
@@ -1354,7 +1354,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.p_full[st]);
-            if (warp == kSoftmaxWarp0 && lane == 0) MLA_BLOCK_STAMP(blk, 4);
+            if ((warp & 3) == 0 && lane == 0) MLA_BLOCK_STAMP(blk, warp == kSoftmaxWarp0 ? 4 : 7);
         }
 
         // ---- epilogue ------------------------------------------------------------------------

@@ -26,9 +26,9 @@ ROOT = os.path.dirname(HERE)
 TRACE_BUILD = os.path.join(HERE, "_build_trace")
 SLOTS = 12          # stamps per CTA (kTraceSlots)
 MAX_CTAS = 8192     # kTraceCtas
-BLOCK_CTAS, BLOCKS, BLOCK_EVENTS = 4, 64, 6   # per-block events of the first CTAs
+BLOCK_CTAS, BLOCKS, BLOCK_EVENTS = 4, 64, 8   # per-block events of the first CTAs
 WORDS = MAX_CTAS * SLOTS + BLOCK_CTAS * BLOCKS * BLOCK_EVENTS
-EVENTS = ["issue", "issued", "qk", "s_read", "p_done", "pv"]
+EVENTS = ["issue", "issued", "qk", "s_read", "p_done", "pv", "s1_read", "p1_done"]
 PHASES = ["start", "waited", "gather0", "qk0", "pv_last", "o_ready", "staged", "stored", "end",
           "q_tile", "mma_go"]
 

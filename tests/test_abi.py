@@ -39,6 +39,29 @@ def test_gather_rate_probe_builds():
     assert os.path.exists(gather_rate.build())
 
 
+def test_trace_tool_matches_the_trace_buffer_layout():
+    # trace.py reads the traced kernel's stamp buffer with its own copy of the
+    # layout constants; they must be the ones the kernel is compiled with
+    import re
+    from split_kv_mla_gb300 import trace
+    hdr = open(os.path.join(os.path.dirname(mla_build.__file__), "csrc",
+                            "mla_internal.h")).read()
+    const = {m.group(1): int(m.group(2))
+             for m in re.finditer(r"constexpr int (kTrace\w+) = (\d+);", hdr)}
+    assert (const["kTraceSlots"], const["kTraceCtas"], const["kTraceBlockCtas"],
+            const["kTraceBlocks"], const["kTraceBlockEvents"]) == (
+        trace.SLOTS, trace.MAX_CTAS, trace.BLOCK_CTAS, trace.BLOCKS, trace.BLOCK_EVENTS)
+    assert len(trace.EVENTS) == trace.BLOCK_EVENTS
+    assert len(trace.PHASES) <= trace.SLOTS
+
+
+@needs_nvcc
+def test_traced_build_compiles():
+    # the clock-stamped build behind the phase timelines compiles for sm_103a
+    from split_kv_mla_gb300 import trace
+    assert os.path.exists(trace.build_traced())
+
+
 def test_every_declared_symbol_is_exported(lib):
     names = mla.declared_symbols()
     assert {"mla_decode_plan", "mla_decode", "mla_sparse_decode", "mla_splitk_reduce",
